@@ -1,0 +1,425 @@
+"""Pins for the CPU oracle: each check fixes the oracle against something other
+than itself (hand-derived fixtures, numpy's and Python's own float16
+conversions, exact integer / rational arithmetic, one-hot inputs, permutation
+invariance, a cross-format reduction, big-integer bit streams)."""
+from __future__ import annotations
+
+import struct
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _fixture(name):
+    rows = []
+    for line in (GOLDEN / name).read_text().splitlines():
+        line = line.split("#", 1)[0].strip()
+        if line:
+            rows.append(line)
+    return rows
+
+
+def _py_half_bits(v: float) -> int:
+    """Python's own binary16 conversion (struct 'e', round-half-even)."""
+    try:
+        return struct.unpack("<H", struct.pack("<e", v))[0]
+    except OverflowError:
+        return 0xFC00 if v < 0 else 0x7C00
+
+
+# ---------------------------------------------------------------- fp16 rounding
+
+def test_fp16_rounding_golden():
+    for row in _fixture("fp16_rounding.txt"):
+        expr, want = row.rsplit(None, 1)
+        v = float(eval(expr, {}, {}))
+        got = int(O.fp16_bits_from_float64(np.array([v]))[0])
+        assert got == int(want, 16), (expr, hex(got), want)
+
+
+def test_fp16_rounding_matches_numpy_random():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(400_000) * np.exp2(rng.integers(-30, 18, 400_000))
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(O.fp16_bits_from_float64(x), want)
+
+
+def test_fp16_rounding_every_tie_and_neighbour():
+    # every fp16 value h, the exact midpoints to its neighbour, and points just
+    # beside them, in every binade including subnormals: compare with numpy and
+    # Python's struct 'e' (both correctly rounded)
+    h = np.arange(0, 0x7C00, dtype=np.uint16)
+    v = O.float64_from_fp16_bits(h)
+    nxt = O.float64_from_fp16_bits(h + 1) if True else None
+    mid = (v + nxt) / 2.0
+    cands = np.concatenate([v, mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf)])
+    cands = np.concatenate([cands, -cands])
+    with np.errstate(over="ignore"):
+        want = cands.astype(np.float16).view(np.uint16)
+    got = O.fp16_bits_from_float64(cands)
+    assert np.array_equal(got, want)
+    sample = cands[:: 997]
+    assert [int(b) for b in O.fp16_bits_from_float64(sample)] == [_py_half_bits(float(c)) for c in sample]
+
+
+def test_fp16_decode_all_patterns():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = O.float64_from_fp16_bits(h)
+    want = h.view(np.float16).astype(np.float64)
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+    assert np.array_equal(got[np.isinf(want)], want[np.isinf(want)])
+
+
+# ---------------------------------------------------------------- GPTQ layout
+
+def test_gptq_golden_words():
+    for row in _fixture("gptq_words.txt"):
+        tok = row.split()
+        word, zero, scale = int(tok[0], 16), int(tok[1]), int(tok[2], 16)
+        want = [int(t, 16) for t in tok[3:]]
+        K = N = 8
+        qweight = np.zeros((1, N), dtype=np.uint32)
+        qweight[0, 0] = word
+        qzeros = np.zeros((1, 1), dtype=np.uint32)
+        qzeros[0, 0] = zero            # nibble 0 = zero of column 0
+        scales = np.zeros((1, N), dtype=np.uint16)
+        scales[0, 0] = scale
+        W = O.dequant_gptq(qweight, qzeros, scales, None, K, 8)
+        assert [int(v) for v in W[:, 0]] == want, tok[0]
+
+
+def test_gptq_zero_nibbles():
+    # zero of column n = 8c + i lives in nibble i of qzeros[g][c]
+    N = 16
+    qz = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    assert O.unpack_gptq_zeros(qz, N)[0].tolist() == list(range(16))
+
+
+@pytest.mark.parametrize("act_order", [False, True])
+def test_gptq_roundtrip_and_definitional(act_order):
+    inp = synth.gptq_layer(256, 48, group_size=32, act_order=act_order, seed=3)
+    qw, qz, sc, perm = O.pack_gptq(inp.q, inp.z, inp.s, inp.g_idx, 32)
+    assert np.array_equal(O.unpack_gptq_codes(qw, 256), inp.q[perm])
+    assert np.array_equal(O.unpack_gptq_zeros(qz, 48), inp.z)
+    # stored rows of group g are the rows of group g
+    assert np.array_equal(inp.g_idx[perm], np.arange(256) // 32)
+    W_packed = O.dequant_gptq(qw, qz, sc, perm, 256, 32)
+    W_def = O.dequant_gptq_definitional(inp.q, inp.z, inp.s, inp.g_idx, 32)
+    assert np.array_equal(W_packed, W_def)
+    cols = np.array([0, 5, 17, 47])
+    assert np.array_equal(O.dequant_gptq(qw, qz, sc, perm, 256, 32, cols=cols), W_def[:, cols])
+
+
+def test_gptq_adversarial_codes_roundtrip():
+    K, N = 64, 16
+    for q in (np.full((K, N), 15, np.uint8), np.zeros((K, N), np.uint8),
+              (np.indices((K, N)).sum(0) % 2 * 15).astype(np.uint8),
+              np.tile(np.array([5, 10], np.uint8), (K, N // 2))):
+        z = np.full((K // 8, N), 7, np.uint8)
+        s = np.full((K // 8, N), 1.0, np.float16)
+        qw, qz, _, perm = O.pack_gptq(q, z, s, None, 8)
+        assert np.array_equal(perm, np.arange(K))
+        assert np.array_equal(O.unpack_gptq_codes(qw, K), q)
+
+
+def test_gptq_stable_sort_tie_break():
+    g_idx = np.array([1, 0, 1, 0, 1, 0, 1, 0] * 2)
+    perm = O.gptq_perm_from_g_idx(g_idx, 8)
+    assert perm.tolist() == [1, 3, 5, 7, 9, 11, 13, 15, 0, 2, 4, 6, 8, 10, 12, 14]
+    with pytest.raises(ValueError):
+        O.gptq_perm_from_g_idx(np.array([0] * 9 + [1] * 7), 8)
+
+
+# ---------------------------------------------------------------- EXL2 layout
+
+def _pattern(spec: str, b: int):
+    i = np.arange(32)
+    if spec.startswith("imod"):
+        return i % int(spec[4:])
+    if spec == "i":
+        return i.copy()
+    pos, val = spec[1:].split("=")
+    out = np.zeros(32, dtype=np.int64)
+    out[int(pos)] = int(val)
+    return out
+
+
+def test_exl2_golden_streams():
+    for row in _fixture("exl2_streams.txt"):
+        tok = row.split()
+        b, spec, words = int(tok[0]), tok[1], [int(t, 16) for t in tok[2:]]
+        codes = _pattern(spec, b).astype(np.uint8)
+        q_st = np.zeros((32, 8), dtype=np.uint8)
+        q_st[:, 3] = codes
+        qw, off, _, _ = O.pack_exl2(q_st, [b], np.ones((1, 8), np.float16), None)
+        assert off.tolist() == [0, b]
+        assert [int(w) for w in qw[:, 3]] == words, (b, spec)
+        assert not qw[:, [0, 1, 2, 4, 5, 6, 7]].any()
+        assert np.array_equal(O.unpack_exl2_codes(qw, [b])[:, 3], codes)
+
+
+def test_exl2_every_value_at_every_position():
+    # brute force: code v at position i of a segment occupies stream bits
+    # [i*b, i*b+b) as the bits of v; built here as one Python big integer
+    for b in O.EXL2_BITS:
+        for i in range(32):
+            for v in {1, (1 << b) - 1, (1 << b) >> 1, 0b101 & ((1 << b) - 1)}:
+                q_st = np.zeros((32, 8), dtype=np.uint8)
+                q_st[i, 0] = v
+                qw, _, _, _ = O.pack_exl2(q_st, [b], np.ones((1, 8), np.float16), None)
+                stream = v << (i * b)
+                want = [(stream >> (32 * t)) & 0xFFFFFFFF for t in range(b)]
+                assert [int(w) for w in qw[:, 0]] == want, (b, i, v)
+                assert int(O.unpack_exl2_codes(qw, [b])[i, 0]) == v
+
+
+def test_exl2_roundtrip_and_definitional():
+    inp = synth.exl2_layer(512, 40, bpw=4.0, seed=5)
+    qw, off, sc, perm = O.pack_exl2(inp.q, inp.bits, inp.s, inp.perm)
+    assert off[-1] == int(inp.bits.astype(int).sum()) == 4 * 16
+    assert np.array_equal(O.unpack_exl2_codes(qw, inp.bits, off), inp.q)
+    W_packed = O.dequant_exl2(qw, off, inp.bits, sc, perm)
+    W_def = O.dequant_exl2_definitional(inp.q, inp.bits, inp.s, inp.perm)
+    assert np.array_equal(W_packed, W_def)
+    cols = np.array([1, 7, 39])
+    assert np.array_equal(O.dequant_exl2(qw, off, inp.bits, sc, perm, cols=cols), W_def[:, cols])
+
+
+def test_exl2_big_integer_packing_random():
+    # the whole packed tensor rebuilt with Python big integers, per column
+    inp = synth.exl2_layer(32 * 6, 8, bits=np.array([2, 3, 4, 5, 6, 8]), seed=9)
+    qw, off, _, _ = O.pack_exl2(inp.q, inp.bits, inp.s, None)
+    for n in range(8):
+        col = []
+        for s_, b in enumerate(inp.bits.tolist()):
+            stream = 0
+            for i in range(32):
+                stream |= int(inp.q[32 * s_ + i, n]) << (i * b)
+            col += [(stream >> (32 * t)) & 0xFFFFFFFF for t in range(b)]
+        assert [int(w) for w in qw[:, n]] == col
+
+
+# ---------------------------------------------------------------- dequant
+
+def test_dequant_exhaustive_vs_numpy():
+    # every (q, z) pair of 4-bit codes and of 8-bit codes against a sweep of
+    # scales (normal, subnormal-producing, overflowing, negative); reference =
+    # numpy's float64 -> float16 cast of the exact product
+    scales = np.array([0.005, 0.0123, 0.02, -0.0177, 2.0 ** -20, -(2.0 ** -24), 3.0 ** -9,
+                       1000.0, 4100.0, -65504.0, 1.0 + 2.0 ** -10, 0.0, -0.0, 0.333], dtype=np.float64)
+    s16 = scales.astype(np.float16)
+    for nbits in (4, 8):
+        qq, zz = np.meshgrid(np.arange(1 << nbits), np.arange(1 << nbits), indexing="ij")
+        d = (qq - zz).reshape(-1, 1).astype(np.float64)
+        prod = d * s16.astype(np.float64).reshape(1, -1)
+        with np.errstate(over="ignore"):
+            want = prod.astype(np.float16).view(np.uint16)
+        got = O.fp16_bits_from_float64(prod)
+        assert np.array_equal(got, want)
+
+
+def test_dequant_exl2_zero_point_is_half_range():
+    # a code equal to 2^(b-1) dequantises to +0 for every width; codes 0 and
+    # 2^b - 1 give -2^(b-1)*s and (2^(b-1)-1)*s
+    for b in O.EXL2_BITS:
+        q_st = np.zeros((32, 8), dtype=np.uint8)
+        q_st[0, :] = 1 << (b - 1)
+        q_st[1, :] = (1 << b) - 1
+        s = np.full((1, 8), 0.5, np.float16)
+        qw, off, sc, _ = O.pack_exl2(q_st, [b], s, None)
+        W = O.float64_from_fp16_bits(O.dequant_exl2(qw, off, [b], sc, None))
+        assert np.all(W[0] == 0) and not np.signbit(W[0]).any()
+        assert np.all(W[1] == ((1 << (b - 1)) - 1) * 0.5)
+        assert np.all(W[2] == -(1 << (b - 1)) * 0.5)
+
+
+def test_rtn_idempotence():
+    # quantize(dequant(q)) == q: fp16 rounding moves w by at most 2^-11 |w|,
+    # i.e. < 0.5 code steps for |q - z| <= 255
+    inp = synth.gptq_layer(128, 32, group_size=32, seed=11)
+    W = O.dequant_gptq_definitional(inp.q, inp.z, inp.s, None, 32)
+    g = np.arange(128) // 32
+    assert np.array_equal(O.quantize_rtn(W, inp.s[g], inp.z[g], 4), inp.q)
+    e = synth.exl2_layer(128, 16, bits=np.array([8, 2, 6, 3]), permute=False, seed=12)
+    W = O.dequant_exl2_definitional(e.q, e.bits, e.s, None)
+    seg = np.arange(128) // 32
+    z = (1 << (e.bits.astype(int)[seg] - 1))[:, None]
+    for b in (8, 2, 6, 3):
+        rows = np.flatnonzero(e.bits[seg] == b)
+        assert np.array_equal(O.quantize_rtn(W[rows], e.s[seg][rows], z[rows], b), e.q[rows])
+
+
+# ---------------------------------------------------------------- matmul
+
+def _exact_int_y(x16, W_bits):
+    """Exact y as Python integers in units of 2^-48 (fp16 values are
+    multiples of 2^-24)."""
+    xi = (O.float64_from_fp16_bits(np.asarray(x16).view(np.uint16)) * 2.0 ** 24).astype(np.int64)
+    wi = (O.float64_from_fp16_bits(W_bits) * 2.0 ** 24).astype(np.int64)
+    M, K = xi.shape
+    N = wi.shape[1]
+    y = [[0] * N for _ in range(M)]
+    xl, wl = xi.tolist(), wi.tolist()
+    for m in range(M):
+        for k in range(K):
+            a = xl[m][k]
+            if a:
+                row = wl[k]
+                ym = y[m]
+                for n in range(N):
+                    ym[n] += a * row[n]
+    return y
+
+
+def test_matmul_vs_exact_integer():
+    inp = synth.gptq_layer(128, 24, group_size=32, act_order=True, seed=21)
+    qw, qz, sc, perm = O.pack_gptq(inp.q, inp.z, inp.s, inp.g_idx, 32)
+    W = O.dequant_gptq(qw, qz, sc, perm, 128, 32)
+    x = synth.activations(3, 128, seed=21)
+    y = O.matmul(x, W)
+    ye = _exact_int_y(x, W)
+    for m in range(3):
+        for n in range(24):
+            exact = ye[m][n] / 2.0 ** 48
+            assert abs(y[m, n] - exact) <= 1e-12 * max(1.0, abs(exact))
+
+
+def test_one_hot_reproduces_rows():
+    inp = synth.exl2_layer(96, 16, bits=np.array([3, 8, 5]), seed=31)
+    qw, off, sc, perm = O.pack_exl2(inp.q, inp.bits, inp.s, inp.perm)
+    W = O.dequant_exl2(qw, off, inp.bits, sc, perm)
+    x = np.zeros((96, 96), dtype=np.float16)
+    x[np.arange(96), np.arange(96)] = 1.0
+    y = O.matmul(x, W)
+    assert np.array_equal(y, O.float64_from_fp16_bits(W))
+    # K != N so a transposed operand cannot pass
+    assert y.shape == (96, 16)
+
+
+def test_permutation_invariance_exact():
+    # apply a random permutation pi to K of both x and W (composed into the
+    # stored->original map): y must not change, exactly
+    K, N, M = 160, 16, 2
+    inp = synth.exl2_layer(K, N, bits=np.array([2, 4, 6, 8, 3]), seed=41)
+    x = synth.activations(M, K, seed=41)
+    qw, off, sc, perm = O.pack_exl2(inp.q, inp.bits, inp.s, inp.perm)
+    W1 = O.dequant_exl2(qw, off, inp.bits, sc, perm)
+    pi = np.random.default_rng(7).permutation(K)
+    x2 = np.empty_like(x)
+    x2[:, pi] = x
+    perm2 = pi[perm]
+    W2 = O.dequant_exl2(qw, off, inp.bits, sc, perm2)
+    assert _exact_int_y(x, W1) == _exact_int_y(x2, W2)
+    assert np.allclose(O.matmul(x, W1), O.matmul(x2, W2), rtol=1e-15, atol=1e-12)
+    # and the same for GPTQ act-order: relabel the original rows
+    g = synth.gptq_layer(K, N, group_size=32, act_order=True, seed=42)
+    q2 = np.empty_like(g.q)
+    q2[pi] = g.q
+    gi2 = np.empty_like(g.g_idx)
+    gi2[pi] = g.g_idx
+    Wa = O.dequant_gptq(*O.pack_gptq(g.q, g.z, g.s, g.g_idx, 32)[:4], K, 32)
+    Wb = O.dequant_gptq(*O.pack_gptq(q2, g.z, g.s, gi2, 32)[:4], K, 32)
+    assert _exact_int_y(x, Wa) == _exact_int_y(x2, Wb)
+
+
+def test_cross_format_exl2_4bit_is_gptq_gs32():
+    # EXL2 with every segment at 4 bits and no permutation is GPTQ with group
+    # size 32, every zero 8 and the same scales: same words, same weights
+    K, N = 128, 16
+    q = synth.gptq_layer(K, N, group_size=32, seed=51).q
+    s = synth.fp16_uniform(np.random.default_rng(5), 0.002, 0.03, (K // 32, N))
+    qw_e, off, sc_e, _ = O.pack_exl2(q, [4] * (K // 32), s, None)
+    z = np.full((K // 32, N), 8, np.uint8)
+    qw_g, qz_g, sc_g, perm = O.pack_gptq(q, z, s, None, 32)
+    assert np.array_equal(qw_e, qw_g)
+    assert np.array_equal(O.dequant_exl2(qw_e, off, [4] * (K // 32), sc_e, None),
+                          O.dequant_gptq(qw_g, qz_g, sc_g, perm, K, 32))
+
+
+def _brute_force_y(x16, Wfun, M, K, N):
+    out = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(float(x16[m, k])) * Fraction(Wfun(k, n))
+            out[m, n] = float(acc)
+    return out
+
+
+def test_brute_force_gptq_8x8_tile():
+    # 8x8 GPTQ tile with group size 8, act-order: weights by the definition in
+    # pure Python (Python's own half conversion), y by exact rationals
+    K = N = 8
+    rng = np.random.default_rng(61)
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, (1, N)).astype(np.uint8)
+    s = synth.fp16_uniform(rng, -0.02, 0.02, (1, N))
+    x = synth.activations(2, K, seed=61)
+    qw, qz, sc, perm = O.pack_gptq(q, z, s, None, 8)
+    y = O.matmul(x, O.dequant_gptq(qw, qz, sc, perm, K, 8))
+
+    def w(k, n):
+        h = _py_half_bits((int(q[k, n]) - int(z[0, n])) * float(s[0, n]))
+        return struct.unpack("<e", struct.pack("<H", h))[0]
+    assert np.allclose(y, _brute_force_y(x, w, 2, K, N), rtol=1e-13, atol=0)
+
+
+def test_brute_force_exl2_32x8_tile():
+    for b in (3, 5, 6):
+        rng = np.random.default_rng(70 + b)
+        q = rng.integers(0, 1 << b, (32, 8)).astype(np.uint8)
+        s = synth.fp16_uniform(rng, 0.002, 0.03, (1, 8))
+        perm = rng.permutation(32).astype(np.int32)
+        x = synth.activations(1, 32, seed=b)
+        qw, off, sc, p = O.pack_exl2(q, [b], s, perm)
+        y = O.matmul(x, O.dequant_exl2(qw, off, [b], sc, p))
+        inv = np.argsort(perm)                       # original row k -> stored row
+
+        def w(k, n):
+            j = inv[k]
+            h = _py_half_bits((int(q[j, n]) - (1 << (b - 1))) * float(s[0, n]))
+            return struct.unpack("<e", struct.pack("<H", h))[0]
+        assert np.allclose(y, _brute_force_y(x, w, 1, 32, 8), rtol=1e-13, atol=0)
+
+
+# ---------------------------------------------------------------- shards
+
+def test_shard_reductions():
+    # column-parallel shards concatenate, row-parallel shards (on segment
+    # boundaries) sum, to the unsharded result
+    inp = synth.exl2_layer(256, 32, bpw=4.0, seed=81, permute=False)
+    x = synth.activations(2, 256, seed=81)
+    qw, off, sc, _ = O.pack_exl2(inp.q, inp.bits, inp.s, None)
+    W = O.dequant_exl2(qw, off, inp.bits, sc, None)
+    y = O.matmul(x, W)
+    cat = np.concatenate([O.matmul(x, O.dequant_exl2(qw, off, inp.bits, sc, None, cols=np.arange(c, c + 16)))
+                          for c in (0, 16)], axis=1)
+    assert np.array_equal(cat, y)
+    ks = []
+    for lo, hi in ((0, 4), (4, 8)):
+        o2 = off[lo:hi + 1] - off[lo]
+        Wk = O.dequant_exl2(qw[off[lo]:off[hi]], o2, inp.bits[lo:hi], sc[lo:hi], None)
+        ks.append(O.matmul(x[:, lo * 32:hi * 32], Wk))
+    assert np.allclose(ks[0] + ks[1], y, rtol=1e-14, atol=1e-12)
+
+
+# ---------------------------------------------------------------- generator
+
+def test_bit_mix_is_exact():
+    for S, bpw, allowed in ((128, 4.0, synth.EXL2_BITS), (344, 4.0, synth.EXL2_BITS),
+                            (256, 2.5, (2, 3, 4)), (896, 2.5, (2, 3, 4))):
+        bits = synth.solve_bit_mix(S, bpw, allowed, np.random.default_rng(S))
+        assert int(bits.astype(int).sum()) == int(bpw * S)
+        assert set(np.unique(bits).tolist()) <= set(allowed)

@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of the dequantize-fused quantized matmul on GB300.
+
+Default workload: the full decode weight stream of a Llama-2-70B-shaped model
+at EXL2 4.0 bpw -- 80 layers x 7 quantized linears (q, k, v, o, gate, up,
+down), M = 1, fresh x ~ N(0,1) per linear, 560 exq_gemv calls back to back
+on one stream, captured once in a CUDA graph. One step = one token = all 560
+GEMVs; the weights (38.5 GB of packed codes + fp16 scales) are far larger
+than L2, so every step streams them from HBM.
+
+Prints one JSON line. ``value`` is the packed-weight throughput (qweight +
+scales bytes per step / time) with everything resident in HBM; ``e2e`` is the
+same metric when each step also copies its 560 activation vectors in from
+pinned host memory and its 560 outputs back; ``roofline`` relates the GEMV
+kernel to the measured HBM copy bandwidth; ``cpu_baseline`` is the CPU oracle
+on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle instead (one bounded sample per
+step) and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode GEMV weight GB/s (% of 8 TB/s); prefill GEMM TFLOPS (% of fp16 peak)"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "decode_stream_70b"
+LINEARS = list(synth.LLAMA2_70B_SHAPES.items())
+GEMV_SOURCES = ["quantized_weight_exq_gb300/csrc/exq_gemv.cu", "quantized_weight_exq_gb300/csrc/exq_device.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="exq", choices=["exq", "reference"])
+    ap.add_argument("--layers", type=int, default=80, help="decoder layers in the stream (80 = Llama-2-70B)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM traffic per algorithmic byte of the GEMV kernel, from the committed
+    ncu summary, or None if that summary was taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "gemv_exl2_decode_70b.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"bench-traffic: dram_bytes_per_algorithmic_byte=([0-9.]+) source_hash=([0-9a-f]+)", txt)
+    if not m or m.group(2) != source_hash(GEMV_SOURCES):
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def bit_mix(layer: int, lin: int, K: int):
+    wid = synth.WORKLOAD_IDS[WORKLOAD]
+    return synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, synth.rng_for(0, wid, 7 * layer + lin, 4))
+
+
+def build_stream(exq, torch, layers: int, device):
+    """Device-resident packed weights for the whole stream. Packed codes are
+    uniform random words (a segment column's b words are a bijection of its
+    32 uniform b-bit codes); bits, scales and permutations follow the EXL2
+    4.0 bpw recipe."""
+    wid = synth.WORKLOAD_IDS[WORKLOAD]
+    lin_list = []
+    x_total = sum(K for _, (K, N) in LINEARS) * layers
+    y_total = sum(N for _, (K, N) in LINEARS) * layers
+    x_all = torch.empty(x_total, dtype=torch.float16, device=device)
+    y_all = torch.empty(y_total, dtype=torch.float16, device=device)
+    xo = yo = 0
+    for layer in range(layers):
+        for i, (name, (K, N)) in enumerate(LINEARS):
+            gen = torch.Generator(device=device)
+            gen.manual_seed(int(synth.rng_for(0, wid, 7 * layer + i, 0).integers(0, 2 ** 62)))
+            bits = bit_mix(layer, i, K)
+            off = np.zeros(bits.size + 1, dtype=np.int64)
+            off[1:] = np.cumsum(bits.astype(np.int64))
+            rows = int(off[-1])
+            qweight = torch.randint(0, 2 ** 32, (rows, N), dtype=torch.int64, device=device,
+                                    generator=gen).to(torch.int32)
+            scales = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
+            perm = torch.randperm(K, device=device, generator=gen).to(torch.int32)
+            w = exq.exl2_weight(qweight, off.astype(np.int32), scales, perm, K, N, device=device)
+            x = x_all[xo:xo + K].view(1, K)
+            x.copy_(torch.randn(1, K, device=device, generator=gen).half())
+            y = y_all[yo:yo + N].view(1, N)
+            xo += K
+            yo += N
+            lin_list.append((w, x, y))
+    return lin_list, x_all, y_all
+
+
+def run_exq(args, rank, world, device):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    lins, x_all, y_all = build_stream(exq, torch, args.layers, device)
+    bytes_per_step = sum(w.packed_bytes for w, _, _ in lins)
+    n_launch = len(lins)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for w, x, y in lins[:len(LINEARS)]:      # settle per-kernel attributes before capture
+            exq.exq_gemv(w, x, y)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for w, x, y in lins:
+                exq.exq_gemv(w, x, y)
+    torch.cuda.synchronize()
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set after warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed(step_fn, steps):
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(steps):
+                step_fn()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return ev0.elapsed_time(ev1)  # ms
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    t_ms = timed(graph.replay, args.steps)
+    clocks = sampler.stop()
+
+    # end to end: activations in from pinned host memory, outputs back, per step
+    x_host = torch.empty_like(x_all, device="cpu").pin_memory()
+    x_host.copy_(x_all.cpu())
+    y_host = torch.empty_like(y_all, device="cpu").pin_memory()
+
+    def e2e_step():
+        x_all.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(y_all, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+    torch.cuda.synchronize()
+    t_e2e_ms = timed(e2e_step, args.steps)
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_ms, t_e2e_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms, t_e2e_ms = float(t[0]), float(t[1])
+
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    gbs = world * bytes_per_step * args.steps / (t_ms * 1e-3) / 1e9
+    e2e_gbs = world * bytes_per_step * args.steps / (t_e2e_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    per_gpu = gbs / world
+    traffic_ratio = profile_traffic()
+    bytes_per_launch = bytes_per_step / n_launch
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": "decode_stream_70b_exl2_4p0bpw",
+            "model_shape": "Llama-2-70B (80 layers x q,k,v,o,gate,up,down)",
+            "layers": args.layers,
+            "M": 1,
+            "bpw": 4.0,
+            "bytes_per_step": bytes_per_step,
+            "gemv_per_step": n_launch,
+            "tokens_per_s": round(1000.0 / (t_ms / args.steps), 2),
+            "pct_of_8TBps": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
+            "l2": "inputs larger than L2 (the packed stream is 38.5 GB per step)",
+            "launch": "one CUDA graph per step, programmatic dependent launch between GEMVs",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(per_gpu, 2),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(per_gpu / peak, 4),
+            "traffic": None if traffic_ratio is None else round(traffic_ratio * bytes_per_launch),
+            "algorithmic_bytes_per_launch": round(bytes_per_launch),
+            "kernel": "gemv_kernel<EXL2, M<=8, act-order>",
+        },
+        "e2e": {
+            "value": round(e2e_gbs, 2),
+            "unit": UNIT,
+            "h2d_bytes_per_step": x_all.numel() * 2,
+            "d2h_bytes_per_step": y_all.numel() * 2,
+        },
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clocks,
+    }
+    return result
+
+
+# ----------------------------------------------------------------------------- oracle
+
+def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 8):
+    """Time the CPU oracle (as it stands) on a bounded sample of the stream:
+    whole k / v projections (8192 x 1024) of the first layers, packed words
+    drawn exactly as in the GPU stream's recipe (numpy side). Runs in this
+    process with numpy; returns (GB/s of packed bytes, seconds, sample text)."""
+    import oracle as O
+
+    wid = synth.WORKLOAD_IDS[WORKLOAD]
+    done_bytes, elapsed, n = 0, 0.0, 0
+    layer = 0
+    while n == 0 or (elapsed < seconds_target and n < max_linears):
+        for i in (1, 2):  # k, v
+            K, N = LINEARS[i][1]
+            bits = bit_mix(layer, i, K)
+            off = O.exl2_seg_word_off(bits)
+            qw = synth.uniform_words(int(off[-1]) * N, seed=0, workload=wid, layer=7 * layer + i).reshape(-1, N)
+            s = synth.fp16_uniform(synth.rng_for(0, wid, 7 * layer + i, 2), 0.002, 0.03, (K // 32, N))
+            perm = synth.rng_for(0, wid, 7 * layer + i, 5).permutation(K).astype(np.int32)
+            x = synth.activations(1, K, seed=0, workload=wid, layer=7 * layer + i)
+            t0 = time.perf_counter()
+            W = O.dequant_exl2(qw, off, bits, s.view(np.uint16), perm)
+            O.matmul(x, W)
+            elapsed += time.perf_counter() - t0
+            done_bytes += qw.nbytes + s.nbytes
+            n += 1
+        layer += 1
+    return done_bytes / elapsed / 1e9, elapsed, f"{n} whole 8192x1024 k/v projections (EXL2 4.0 bpw, M=1)"
+
+
+def cpu_baseline_subprocess():
+    """Run the oracle timing in a fresh single-threaded process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "g, t, s = bench.oracle_sample_gbs(); print(json.dumps([g, t, s]))") % ROOT
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return None
+    g, t, s = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(g, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{s}; {t:.1f} s of CPU work, numpy float64, single thread"}
+
+
+def run_reference(args):
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    res = []
+    for _ in range(args.warmup):
+        oracle_sample_gbs(seconds_target=0.0, max_linears=2)
+    t_total, b_total = 0.0, 0.0
+    for _ in range(args.steps):
+        g, t, _ = oracle_sample_gbs(seconds_target=0.0, max_linears=2)
+        t_total += t
+        b_total += g * t * 1e9
+        res.append(g)
+    gbs = b_total / t_total / 1e9
+    sample = "2 whole 8192x1024 k/v projections of the 70B EXL2 4.0 bpw stream per step (M=1)"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 4),
+        "unit": UNIT,
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1000 * t_total / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode_stream_70b_exl2_4p0bpw", "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    result = run_exq(args, rank, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_subprocess()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * exq.h -- C ABI of libexq, a dequantize-fused quantized matmul for sm_103a.
+ *
+ *   y[M, N] = x[M, K] . dequant(Wq)[K, N]      fp16 in, fp32 accumulate, fp16 out
+ *
+ * Two weight formats, as described by the ExLlamaV2 pages:
+ *
+ *  GPTQ 4-bit: group-wise codes q in 0..15, one fp16 scale s and one 4-bit
+ *    zero z per (group, output column), w = (q - z) * s. Optional act-order:
+ *    g_idx[k] assigns each input row k to a group; rows are stored sorted by
+ *    group and a permutation maps stored rows back to input features.
+ *    (ExLlamaV2 blog post "ExLlamaV2: The fastest inference engine for
+ *    quantized Llama/HF models", section "How the Fused CUDA Kernel Works";
+ *    ExLlamaV2 README, "Performance" table, act-order column.)
+ *
+ *  EXL2: rows are cut into 32-row segments, each packed at its own width
+ *    b in {2,3,4,5,6,8}; symmetric codes, w = (q - 2^(b-1)) * s with one fp16
+ *    scale per (segment, output column); a row permutation maps stored rows
+ *    to input features. (ExLlamaV2 README, section "EXL2 quantization";
+ *    blog post, "Step 3: Quantization Application".)
+ *
+ * Packed layouts (fixed by this library; the pages leave them open):
+ *  - qweight is uint32 [n_word_rows, N], N contiguous (row-major), packing
+ *    runs along K, least-significant bits first.
+ *  - GPTQ: stored row j = 8r + i is nibble i (bits 4i..4i+3) of qweight[r][n].
+ *    qzeros is uint32 [G, N/8]: zero of column n = 8c + i is nibble i of
+ *    qzeros[g][c]. scales fp16 [G, N]. Group of stored row j is j / group_size.
+ *  - EXL2: segment s occupies word rows [seg_word_off[s], seg_word_off[s+1]);
+ *    its width is b = seg_word_off[s+1] - seg_word_off[s]. For column n the
+ *    segment's 32 codes form a 32*b-bit stream, code i at stream bits
+ *    [i*b, i*b+b), stream bit p is bit (p mod 32) of word row
+ *    seg_word_off[s] + p/32. scales fp16 [S, N].
+ *  - perm int32 [K] (optional): perm[j] = input feature (row of x's K axis
+ *    and of the dequantized W) held by stored row j.
+ *  - Dequantized weight: w = fp16_round_to_nearest_even((q - z) * s), computed
+ *    with exactly one rounding.
+ *
+ * Conventions for every call below:
+ *  - Device pointers are BORROWED: the caller allocates, owns and frees them.
+ *    The library never allocates device or host memory and keeps no state
+ *    between calls except one device-side error word.
+ *  - Device calls are asynchronous on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream) and never synchronise.
+ *  - Argument checks run on the host before any launch; a failed check
+ *    returns EXQ_ERR_INVALID_ARG or EXQ_ERR_UNSUPPORTED and launches nothing.
+ *    A failed launch returns EXQ_ERR_CUDA.
+ *  - Kernels that wait on on-chip barriers give up after a bounded time,
+ *    record EXQ_ERR_TIMEOUT in the device error word and return; read it with
+ *    exq_get_last_device_error().
+ *  - Device pointers must be 16-byte aligned; N % 8 == 0; GPTQ needs
+ *    K % group_size == 0 and group_size % 32 == 0; EXL2 needs K % 32 == 0.
+ *  - fp16 values travel as their uint16 bit patterns.
+ */
+#ifndef EXQ_H
+#define EXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EXQ_OK = 0,
+  EXQ_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or layout        */
+  EXQ_ERR_UNSUPPORTED = 2, /* valid, but outside what this build handles    */
+  EXQ_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+  EXQ_ERR_TIMEOUT = 4      /* a device-side wait gave up (from the device)  */
+} exq_status;
+
+typedef enum { EXQ_FMT_GPTQ4 = 1, EXQ_FMT_EXL2 = 2 } exq_format;
+
+/* Plain descriptor of one packed linear layer. Every pointer is a borrowed
+ * DEVICE pointer. */
+typedef struct {
+  int32_t format;      /* exq_format                                          */
+  int32_t K;           /* input features (rows of W)                          */
+  int32_t N;           /* output features (columns of W)                      */
+  int32_t group_size;  /* GPTQ: rows per group (multiple of 32); EXL2: 32     */
+  int32_t n_groups;    /* GPTQ: G = K / group_size; EXL2: S = K / 32           */
+  int32_t n_word_rows; /* rows of qweight: GPTQ K / 8; EXL2 sum of widths     */
+  const uint32_t* qweight;      /* [n_word_rows, N]                           */
+  const uint16_t* scales;       /* fp16 [n_groups, N]                         */
+  const uint32_t* qzeros;       /* GPTQ: [G, N/8]; EXL2: NULL                 */
+  const int32_t* perm;          /* [K] stored row -> input feature, or NULL   */
+  const uint32_t* seg_word_off; /* EXL2: [S + 1] word-row prefix sums; GPTQ: NULL */
+} exq_weight;
+
+/* ---------------------------------------------------------------- packers */
+
+/* exq_pack_gptq -- host-only, synchronous, no CUDA.
+ * Packs a GPTQ layer (ExLlamaV2 blog post, "How the Fused CUDA Kernel Works":
+ * eight 4-bit codes per uint32, least-significant nibble first).
+ *   q      [K, N] uint8 codes 0..15, rows in input-feature order (host)
+ *   z      [G, N] uint8 zero points 0..15 (host), G = K / group_size
+ *   g_idx  [K] group of each input row, or NULL for k / group_size (host).
+ *          Every group must hold exactly group_size rows.
+ *   qweight_out [K/8, N], qzeros_out [G, N/8], perm_out [K] (host, caller-
+ *          allocated). Rows are stored sorted stably by (g_idx[k], k) and
+ *          perm_out[j] is the input row of stored row j. The fp16 scales
+ *          [G, N] need no packing and are used as they are.
+ * Returns EXQ_ERR_INVALID_ARG for NULL buffers, K % group_size, N % 8,
+ * K % 8, a code or zero above 15, or a malformed g_idx; outputs are then
+ * unspecified. */
+exq_status exq_pack_gptq(const uint8_t* q, const uint8_t* z, const int32_t* g_idx,
+                         int32_t K, int32_t N, int32_t group_size,
+                         uint32_t* qweight_out, uint32_t* qzeros_out, int32_t* perm_out);
+
+/* exq_pack_exl2 -- host-only, synchronous, no CUDA.
+ * Packs an EXL2 layer (ExLlamaV2 README, "EXL2 quantization"; blog post,
+ * "Step 3: Quantization Application") into the segment bit streams above.
+ *   q      [K, N] uint8 codes in STORED row order, code < 2^bits[j/32] (host)
+ *   bits   [S] widths in {2,3,4,5,6,8}, S = K / 32 (host)
+ *   qweight_out [sum(bits), N] (host, caller-allocated; size from
+ *          exq_exl2_word_rows), seg_word_off_out [S + 1] (host).
+ * The fp16 scales [S, N] and the permutation need no packing.
+ * Returns EXQ_ERR_INVALID_ARG for NULL buffers, K % 32, N % 8, a width
+ * outside the set or a code that does not fit its width. */
+exq_status exq_pack_exl2(const uint8_t* q, const uint8_t* bits, int32_t K, int32_t N,
+                         uint32_t* qweight_out, uint32_t* seg_word_off_out);
+
+/* Number of qweight rows an EXL2 layer needs: sum of bits[0..n_segments).
+ * Returns -1 if bits is NULL, n_segments <= 0 or a width is outside the set. */
+int64_t exq_exl2_word_rows(const uint8_t* bits, int32_t n_segments);
+
+/* ---------------------------------------------------------------- device ops */
+
+/* exq_dequant -- W_out[perm[j]][n] = w(j, n) for every stored row j, i.e. the
+ * dense fp16 weight [K, N] in input-feature order, bit-exact to the
+ * definition above (the "dequantize first" path the ExLlamaV2 blog post,
+ * "Finding 2", contrasts with the fused kernel).
+ *   w      descriptor with device pointers (host struct, read during the call)
+ *   W_out  device fp16 [K, N], caller-allocated, fully overwritten */
+exq_status exq_dequant(const exq_weight* w, uint16_t* W_out, void* stream);
+
+/* exq_gemv -- decode-sized fused matmul, 1 <= M <= 16 (ExLlamaV2 blog post,
+ * "How the Fused CUDA Kernel Works": the packed weights are read once,
+ * dequantized in registers and multiplied into fp32 sums).
+ *   x  device fp16 [M, K] row-major, input-feature order
+ *   y  device fp16 [M, N] row-major, fully overwritten
+ * Needs no workspace. Deterministic: the same inputs give the same bits.
+ * Returns EXQ_ERR_UNSUPPORTED for M > 16 (use exq_gemm). */
+exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
+
+/* Bytes of device workspace exq_gemm needs for this layer and M (0 if none;
+ * a permuted layer needs M * K * 2 bytes for the gathered activations). */
+size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M);
+
+/* exq_gemm -- prefill-sized fused matmul for any M >= 1 (tuned for M >= 128):
+ * packed tiles are dequantized to fp16 in shared memory and fed to the
+ * tcgen05 tensor cores with fp32 accumulation in tensor memory.
+ *   x  device fp16 [M, K], y device fp16 [M, N] (fully overwritten)
+ *   workspace  device buffer of at least exq_gemm_workspace_size() bytes
+ *              (may be NULL when that size is 0); contents are scratch.
+ * Requires K % 64 == 0 and N % 128 == 0 in addition to the rules above,
+ * else EXQ_ERR_UNSUPPORTED. */
+exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Static, NUL-terminated description of a status code. */
+const char* exq_status_string(exq_status s);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: EXQ_OK, EXQ_ERR_TIMEOUT (a kernel gave up waiting) or
+ * EXQ_ERR_INVALID_ARG (a kernel met an EXL2 segment width outside the set).
+ * Returns EXQ_ERR_CUDA if the synchronisation itself fails. */
+exq_status exq_get_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXQ_H */

@@ -1,0 +1,115 @@
+// Host entry points of libexq: argument checks, dispatch, status codes.
+// Every check here runs before any launch and has no side effects.
+#include <cstdint>
+#include <mutex>
+
+#include "exq_internal.h"
+
+namespace exq {
+
+const DeviceInfo& device_info(int device) {
+  constexpr int kMaxDevices = 64;
+  static DeviceInfo infos[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  static DeviceInfo none;
+  if (device < 0 || device >= kMaxDevices) return none;
+  std::call_once(once[device], [device] {
+    DeviceInfo d;
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, device);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, device);
+    infos[device] = d;
+  });
+  return infos[device];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// structural checks of a layer descriptor (host-visible fields only)
+exq_status check_weight(const exq_weight* w) {
+  if (!w) return EXQ_ERR_INVALID_ARG;
+  if (w->K <= 0 || w->N <= 0 || w->N % 8 || w->K % 32) return EXQ_ERR_INVALID_ARG;
+  if (!w->qweight || !w->scales || !aligned16(w->qweight) || !aligned16(w->scales)) return EXQ_ERR_INVALID_ARG;
+  if (w->perm && !aligned16(w->perm)) return EXQ_ERR_INVALID_ARG;
+  if (w->format == EXQ_FMT_GPTQ4) {
+    if (w->group_size <= 0 || w->group_size % 32 || w->K % w->group_size) return EXQ_ERR_INVALID_ARG;
+    if (w->n_groups != w->K / w->group_size || w->n_word_rows != w->K / 8) return EXQ_ERR_INVALID_ARG;
+    if (!w->qzeros || !aligned16(w->qzeros) || w->seg_word_off) return EXQ_ERR_INVALID_ARG;
+  } else if (w->format == EXQ_FMT_EXL2) {
+    if (w->group_size != 32 || w->n_groups != w->K / 32) return EXQ_ERR_INVALID_ARG;
+    if (w->n_word_rows < 2 * w->n_groups || w->n_word_rows > 8 * w->n_groups) return EXQ_ERR_INVALID_ARG;
+    if (!w->seg_word_off || w->qzeros) return EXQ_ERR_INVALID_ARG;
+  } else {
+    return EXQ_ERR_INVALID_ARG;
+  }
+  return EXQ_OK;
+}
+
+int current_cc() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  const DeviceInfo& di = device_info(dev);
+  return di.cc_major * 10 + di.cc_minor;
+}
+
+}  // namespace
+}  // namespace exq
+
+using namespace exq;
+
+extern "C" exq_status exq_dequant(const exq_weight* w, uint16_t* W_out, void* stream) {
+  const exq_status st = check_weight(w);
+  if (st != EXQ_OK) return st;
+  if (!W_out || !aligned16(W_out)) return EXQ_ERR_INVALID_ARG;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_dequant(*w, W_out, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream) {
+  const exq_status st = check_weight(w);
+  if (st != EXQ_OK) return st;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
+  if (M > 16) return EXQ_ERR_UNSUPPORTED;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_gemv(*w, x, M, y, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M) {
+  if (check_weight(w) != EXQ_OK || M < 1) return 0;
+  return gemm_workspace_bytes(*w, M);
+}
+
+extern "C" exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  const exq_status st = check_weight(w);
+  if (st != EXQ_OK) return st;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
+  const size_t need = gemm_workspace_bytes(*w, M);
+  if (need && (!workspace || ws_bytes < need || !aligned16(workspace))) return EXQ_ERR_INVALID_ARG;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_gemm(*w, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char* exq_status_string(exq_status s) {
+  switch (s) {
+    case EXQ_OK: return "ok";
+    case EXQ_ERR_INVALID_ARG: return "invalid argument";
+    case EXQ_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case EXQ_ERR_CUDA: return "CUDA error";
+    case EXQ_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+extern "C" exq_status exq_get_last_device_error(void* stream) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned a = take_gemv_errors(s), b = take_dequant_errors(s), c = take_gemm_errors(s);
+  if (a == ~0u || b == ~0u || c == ~0u) return EXQ_ERR_CUDA;
+  const unsigned v = a | b | c;
+  if (v & kDevErrTimeout) return EXQ_ERR_TIMEOUT;
+  if (v & kDevErrBadSegment) return EXQ_ERR_INVALID_ARG;
+  return EXQ_OK;
+}

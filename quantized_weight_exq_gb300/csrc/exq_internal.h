@@ -1,0 +1,38 @@
+// Internal interfaces between the host entry points (exq_api.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "exq.h"
+
+namespace exq {
+
+// device error codes recorded by kernels (OR-ed into a per-module word)
+enum : unsigned {
+  kDevErrTimeout = 1u,      // a bounded wait gave up
+  kDevErrBadSegment = 2u,   // an EXL2 segment width outside {2,3,4,5,6,8} or past the end
+};
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+// queried once per device, cached (host-only, thread-safe)
+const DeviceInfo& device_info(int device);
+
+exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream);
+exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t stream);
+exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+size_t gemm_workspace_bytes(const exq_weight& w, int M);
+
+// read-and-clear of each module's device error word (stream-ordered copy +
+// synchronise); returns the OR of the codes or ~0u on a CUDA failure
+unsigned take_gemv_errors(cudaStream_t stream);
+unsigned take_dequant_errors(cudaStream_t stream);
+unsigned take_gemm_errors(cudaStream_t stream);
+
+}  // namespace exq

@@ -1,0 +1,229 @@
+"""Python binding of libexq (ctypes): argument marshalling only.
+
+Every function here forwards to the C ABI in ``include/exq.h`` with the same
+name; all arithmetic runs in the library (host packers in C++, device ops in
+CUDA kernels). torch is used only to hold device memory and to name the
+current CUDA stream. If ``libexq.so`` has not been built, importing this
+module raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+from pathlib import Path
+from typing import Optional
+
+import numpy as np
+
+_LIB_PATH = Path(__file__).resolve().parent / "libexq.so"
+
+EXQ_OK = 0
+EXQ_ERR_INVALID_ARG = 1
+EXQ_ERR_UNSUPPORTED = 2
+EXQ_ERR_CUDA = 3
+EXQ_ERR_TIMEOUT = 4
+
+EXQ_FMT_GPTQ4 = 1
+EXQ_FMT_EXL2 = 2
+
+# every symbol include/exq.h declares
+EXPORTED = (
+    "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv",
+    "exq_gemm_workspace_size", "exq_gemm", "exq_status_string", "exq_get_last_device_error",
+)
+
+
+class ExqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class exq_weight(ctypes.Structure):
+    _fields_ = [
+        ("format", ctypes.c_int32), ("K", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("group_size", ctypes.c_int32), ("n_groups", ctypes.c_int32), ("n_word_rows", ctypes.c_int32),
+        ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("qzeros", ctypes.c_void_p),
+        ("perm", ctypes.c_void_p), ("seg_word_off", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    if not _LIB_PATH.exists():
+        raise ImportError(f"{_LIB_PATH} is not built; run quantized_weight_exq_gb300/build.py "
+                          "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P, i32, i64, sz, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    W = ctypes.POINTER(exq_weight)
+    sig = {
+        "exq_pack_gptq": (st, [P, P, P, i32, i32, i32, P, P, P]),
+        "exq_pack_exl2": (st, [P, P, i32, i32, P, P]),
+        "exq_exl2_word_rows": (i64, [P, i32]),
+        "exq_dequant": (st, [W, P, P]),
+        "exq_gemv": (st, [W, P, i32, P, P]),
+        "exq_gemm_workspace_size": (sz, [W, i32]),
+        "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
+        "exq_status_string": (ctypes.c_char_p, [st]),
+        "exq_get_last_device_error": (st, [P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return str(_LIB_PATH)
+
+
+def status_string(status: int) -> str:
+    return _lib.exq_status_string(int(status)).decode()
+
+
+exq_status_string = status_string
+
+
+def _check(status: int, where: str):
+    if status != EXQ_OK:
+        raise ExqError(status, where)
+
+
+def _np_ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- host packers
+
+def exq_pack_gptq(q: np.ndarray, z: np.ndarray, g_idx: Optional[np.ndarray], group_size: int):
+    """-> (qweight uint32 [K/8, N], qzeros uint32 [G, N/8], perm int32 [K])."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    z = np.ascontiguousarray(z, dtype=np.uint8)
+    K, N = q.shape
+    gi = None if g_idx is None else np.ascontiguousarray(g_idx, dtype=np.int32)
+    qweight = np.empty((K // 8, N), dtype=np.uint32)
+    qzeros = np.empty((max(K // max(group_size, 1), 1), N // 8), dtype=np.uint32)
+    perm = np.empty(K, dtype=np.int32)
+    _check(_lib.exq_pack_gptq(_np_ptr(q), _np_ptr(z), _np_ptr(gi), K, N, group_size,
+                              _np_ptr(qweight), _np_ptr(qzeros), _np_ptr(perm)), "exq_pack_gptq")
+    return qweight, qzeros, perm
+
+
+def exq_exl2_word_rows(bits: np.ndarray) -> int:
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    return int(_lib.exq_exl2_word_rows(_np_ptr(bits), bits.size))
+
+
+def exq_pack_exl2(q: np.ndarray, bits: np.ndarray):
+    """-> (qweight uint32 [sum(bits), N], seg_word_off uint32 [S + 1])."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    K, N = q.shape
+    rows = exq_exl2_word_rows(bits)
+    if rows < 0:
+        raise ExqError(EXQ_ERR_INVALID_ARG, "exq_pack_exl2")
+    qweight = np.empty((rows, N), dtype=np.uint32)
+    off = np.empty(bits.size + 1, dtype=np.uint32)
+    _check(_lib.exq_pack_exl2(_np_ptr(q), _np_ptr(bits), K, N, _np_ptr(qweight), _np_ptr(off)), "exq_pack_exl2")
+    return qweight, off
+
+
+# ---------------------------------------------------------------- device layer
+
+@dataclass
+class Weight:
+    """A packed layer resident on the GPU (torch tensors hold the memory)."""
+
+    format: int
+    K: int
+    N: int
+    group_size: int
+    qweight: "object"                 # torch.int32 [rows, N] (uint32 bits)
+    scales: "object"                  # torch.float16 [G or S, N]
+    qzeros: "object" = None           # torch.int32 [G, N/8] (GPTQ)
+    perm: "object" = None             # torch.int32 [K]
+    seg_word_off: "object" = None     # torch.int32 [S + 1] (EXL2)
+    _desc: exq_weight = field(default=None, repr=False)
+
+    def desc(self) -> exq_weight:
+        if self._desc is None:
+            ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+            self._desc = exq_weight(
+                self.format, self.K, self.N, self.group_size, self.scales.shape[0], self.qweight.shape[0],
+                ptr(self.qweight), ptr(self.scales), ptr(self.qzeros), ptr(self.perm), ptr(self.seg_word_off))
+        return self._desc
+
+    @property
+    def packed_bytes(self) -> int:
+        """qweight + scales + qzeros bytes (the weight stream of one matmul)."""
+        n = self.qweight.numel() * 4 + self.scales.numel() * 2
+        if self.qzeros is not None:
+            n += self.qzeros.numel() * 4
+        return n
+
+
+def _dev(a, dtype, device):
+    import torch
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        return a.to(device=device).contiguous()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        a = a.view(np.int32)
+    if a.dtype == np.uint16:
+        a = a.view(np.float16)
+    return torch.from_numpy(a).to(device=device, dtype=dtype).contiguous()
+
+
+def gptq_weight(qweight, qzeros, scales, perm, K: int, N: int, group_size: int, device="cuda") -> Weight:
+    import torch
+    return Weight(EXQ_FMT_GPTQ4, K, N, group_size, _dev(qweight, torch.int32, device),
+                  _dev(scales, torch.float16, device), _dev(qzeros, torch.int32, device),
+                  _dev(perm, torch.int32, device), None)
+
+
+def exl2_weight(qweight, seg_word_off, scales, perm, K: int, N: int, device="cuda") -> Weight:
+    import torch
+    return Weight(EXQ_FMT_EXL2, K, N, 32, _dev(qweight, torch.int32, device),
+                  _dev(scales, torch.float16, device), None, _dev(perm, torch.int32, device),
+                  _dev(seg_word_off, torch.int32, device))
+
+
+def exq_dequant(w: Weight, W_out, stream=None):
+    _check(_lib.exq_dequant(ctypes.byref(w.desc()), W_out.data_ptr(), _stream_ptr(stream)), "exq_dequant")
+    return W_out
+
+
+def exq_gemv(w: Weight, x, y, stream=None):
+    _check(_lib.exq_gemv(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), _stream_ptr(stream)),
+           "exq_gemv")
+    return y
+
+
+def exq_gemm_workspace_size(w: Weight, M: int) -> int:
+    return int(_lib.exq_gemm_workspace_size(ctypes.byref(w.desc()), M))
+
+
+def exq_gemm(w: Weight, x, y, workspace=None, stream=None):
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.exq_gemm(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), ws_ptr, ws_bytes,
+                         _stream_ptr(stream)), "exq_gemm")
+    return y
+
+
+def exq_get_last_device_error(stream=None) -> int:
+    return int(_lib.exq_get_last_device_error(_stream_ptr(stream)))

@@ -1,0 +1,114 @@
+"""CPU-side checks of the C ABI: the library loads without a GPU, exports
+every symbol include/exq.h declares, its host packers match the oracle's
+packers bit for bit, and host-side argument checks reject bad input before
+anything reaches CUDA."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def exq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as m
+    return m
+
+
+def test_library_exports_every_declared_symbol(exq):
+    header = (ROOT / "include" / "exq.h").read_text()
+    header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    declared = set(re.findall(r"\b(exq_[a-z0-9_]+)\s*\(", header))
+    assert declared == set(exq.EXPORTED), declared ^ set(exq.EXPORTED)
+    lib = ctypes.CDLL(exq.library_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(exq):
+    for s in range(5):
+        assert exq.status_string(s) and "unknown" not in exq.status_string(s)
+    assert "unknown" in exq.status_string(99)
+
+
+@pytest.mark.parametrize("act_order,gs", [(False, 128), (True, 128), (True, 32), (False, 64)])
+def test_pack_gptq_matches_oracle(exq, act_order, gs):
+    g = synth.gptq_layer(512, 72, gs, act_order=act_order, seed=gs)
+    qw, qz, perm = exq.exq_pack_gptq(g.q, g.z, g.g_idx, gs)
+    oqw, oqz, _, operm = O.pack_gptq(g.q, g.z, g.s, g.g_idx, gs)
+    assert np.array_equal(perm, operm)
+    assert np.array_equal(qw, oqw)
+    assert np.array_equal(qz, oqz)
+
+
+def test_pack_exl2_matches_oracle(exq):
+    for seed, bits in ((1, None), (2, np.array([8, 2, 3, 6, 5, 4] * 3))):
+        e = synth.exl2_layer(32 * 18, 40, bpw=4.0, bits=bits, seed=seed)
+        qw, off = exq.exq_pack_exl2(e.q, e.bits)
+        oqw, ooff, _, _ = O.pack_exl2(e.q, e.bits, e.s, e.perm)
+        assert np.array_equal(off, ooff)
+        assert np.array_equal(qw, oqw)
+        assert exq.exq_exl2_word_rows(e.bits) == int(e.bits.astype(int).sum())
+
+
+def test_packers_reject_bad_input(exq):
+    q = np.zeros((64, 8), np.uint8)
+    z = np.zeros((2, 8), np.uint8)
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_gptq(np.full((64, 8), 16, np.uint8), z, None, 32)   # code > 15
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_gptq(q, z, np.array([0] * 33 + [1] * 31, np.int32), 32)  # unequal groups
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_gptq(q[:, :6], z[:, :6], None, 32)  # N % 8
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_exl2(np.full((64, 8), 4, np.uint8), np.array([2, 2], np.uint8))  # code too wide
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_exl2(q, np.array([2, 7], np.uint8))  # width outside the set
+    assert exq.exq_exl2_word_rows(np.array([2, 7], np.uint8)) == -1
+
+
+def _desc(exq, **kw):
+    base = dict(format=exq.EXQ_FMT_GPTQ4, K=256, N=64, group_size=128, n_groups=2, n_word_rows=32,
+                qweight=0x10000, scales=0x20000, qzeros=0x30000, perm=None, seg_word_off=None)
+    base.update(kw)
+    return exq.exq_weight(*[base[f] for f, _ in exq.exq_weight._fields_])
+
+
+def test_device_entry_points_validate_on_host(exq):
+    from quantized_weight_exq_gb300 import exq as mod
+    lib = mod._lib
+    bad = [
+        dict(N=60),                        # N % 8
+        dict(K=250),                       # K % 32
+        dict(group_size=48),               # group % 32
+        dict(n_groups=3),                  # inconsistent G
+        dict(qweight=0x10004),             # misaligned
+        dict(qzeros=None),                 # GPTQ without zeros
+        dict(format=7),                    # unknown format
+        dict(format=2, group_size=32, n_groups=8, n_word_rows=32, qzeros=None, seg_word_off=None),
+        dict(format=2, group_size=32, n_groups=8, n_word_rows=100, qzeros=None, seg_word_off=0x40000),
+    ]
+    for kw in bad:
+        d = _desc(exq, **kw)
+        assert lib.exq_gemv(ctypes.byref(d), 0x50000, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG, kw
+        assert lib.exq_dequant(ctypes.byref(d), 0x60000, None) == exq.EXQ_ERR_INVALID_ARG, kw
+        assert lib.exq_gemm(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
+    d = _desc(exq)
+    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 17, 0x60000, None) == exq.EXQ_ERR_UNSUPPORTED
+    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 0, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_gemv(ctypes.byref(d), 0x50008, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_gemv(None, 0x50000, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
+    # act-order prefill needs a workspace for the gathered activations
+    dp = _desc(exq, perm=0x70000)
+    assert lib.exq_gemm_workspace_size(ctypes.byref(dp), 128) == 128 * 256 * 2
+    assert lib.exq_gemm(ctypes.byref(dp), 0x50000, 128, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG

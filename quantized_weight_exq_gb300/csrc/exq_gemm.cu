@@ -1,18 +1,527 @@
-// Prefill-sized fused quantized matmul (tcgen05). Placeholder until the
-// tensor-memory kernel is in place: reports the shape as unsupported.
+// Prefill-sized fused quantized matmul on the 5th-generation tensor cores:
+//   y[M, N] = x[M, K] . dequant(Wq)[K, N], fp16 in, fp32 accumulate, fp16 out.
+//
+// The ExLlamaV2 blog post ("ExLlamaV2: The fastest inference engine for
+// quantized Llama/HF models", section "How the Fused CUDA Kernel Works")
+// describes the fused kernel as loading packed weights, dequantising on the
+// fly and doing the matmul in the same kernel without an intermediate write,
+// "using tensor cores". Here that becomes, per 128 x 256 output tile:
+//
+//   warp 0      TMA producer: the x tile (128 x 64 fp16, 128-byte swizzle)
+//               through a tensor map, and the packed word rows, scales and
+//               zeros of the 64-row K slab as 1-D bulk copies (EXL2 segments
+//               have data-dependent row counts, which fixed TMA boxes cannot
+//               express), all completing on one mbarrier per stage.
+//   warps 2-9   dequantisers: packed words -> exact fp16 (q - z) -> * s, one
+//               output column per thread, written to shared memory as the
+//               K-major, 128-byte-swizzled B operand; then the epilogue.
+//   warp 1      allocates tensor memory; one elected lane issues
+//               tcgen05.mma.kind::f16 (M=128, N=256, K=16) x 4 per stage,
+//               accumulating fp32 in TMEM, and commits each stage back to its
+//               "empty" mbarrier.
+//   epilogue    tcgen05.ld 32x32b -> fp16 -> global.
+//
+// Act-order (a stored-row permutation) is applied to x by a gather kernel
+// into the caller's workspace first, so the tensor map reads x in stored-row
+// order. Every mbarrier wait is bounded; on expiry the kernel records a
+// timeout in its device error word, drains its own copies and frees TMEM.
+#include <cuda.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "exq_device.cuh"
 #include "exq_internal.h"
 
 namespace exq {
 namespace {
+
 __device__ unsigned g_gemm_err;
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 3;
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = (2 + kDequantWarps) * 32;
+
+// per-stage shared memory layout (bytes)
+constexpr int kXBytes = BM * BK * 2;        // 16 KB, 1024-aligned
+constexpr int kBBytes = BN * BK * 2;        // 32 KB, 1024-aligned
+constexpr int kPackedBytes = 16 * BN * 4;   // up to 16 word rows (two 8-bit segments)
+constexpr int kScaleBytes = 2 * BN * 2;     // two 32-row halves
+constexpr int kZeroBytes = 2 * (BN / 8) * 4;
+constexpr int kOffX = 0;
+constexpr int kOffB = kOffX + kXBytes;
+constexpr int kOffPacked = kOffB + kBBytes;
+constexpr int kOffScale = kOffPacked + kPackedBytes;
+constexpr int kOffZero = kOffScale + kScaleBytes;
+constexpr int kStageBytes = ((kOffZero + kZeroBytes + 1023) / 1024) * 1024;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kTmemCols = 256;
+constexpr long long kWaitLimit = 1ll << 22;  // try_wait rounds before giving up
+
+struct GemmArgs {
+  const uint32_t* qweight;
+  const uint16_t* scales;
+  const uint32_t* qzeros;
+  const uint32_t* seg_off;
+  uint16_t* y;
+  int M, N, K, gs, n_word_rows, fmt;
+};
+
+struct StageMeta {  // written by the producer before the stage's copies
+  int rows0, rows1;  // word rows of the two 32-row halves (EXL2 widths; GPTQ 4, 4)
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait; returns false (and records a timeout) if the phase never completes
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  atomicOr(&g_gemm_err, kDevErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+// Bounded wait by a whole warp: every lane polls, and the loop exits for all
+// lanes in the same round, so warp-collective instructions that follow
+// (tcgen05.ld.sync.aligned, __syncwarp) are always reached convergently.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    const bool done = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+  }
+  if ((threadIdx.x & 31) == 0) atomicOr(&g_gemm_err, kDevErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);        // start address
+  d |= static_cast<uint64_t>(1) << 16;                        // leading byte offset (unused for SW128 K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                        // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                        // swizzle: 128B
+  return d;
+}
+
+// instruction descriptor: D fp32, A/B fp16, both K-major, M = 128, N = 256
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool valid_width(int b) {
+  return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8;
+}
+
+// 8 codes of one column, dequantised, in natural K order (k0, k1), ..., (k6, k7)
+__device__ __forceinline__ uint4 natural_order(const uint32_t (&P)[4]) {
+  uint4 o;
+  o.x = prmt(P[0], P[1], 0x5410);
+  o.y = prmt(P[2], P[3], 0x5410);
+  o.z = prmt(P[0], P[1], 0x7632);
+  o.w = prmt(P[2], P[3], 0x7632);
+  return o;
+}
+
+template <int B>
+__device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col, uint32_t s2) {
+  int wi, off;
+  block_window(B, t, wi, off);
+  const uint32_t wa = rows[wi * BN + col];
+  const uint32_t wb = block_needs_second(B, off) ? rows[(wi + 1) * BN + col] : 0u;
+  uint32_t P[4];
+  unpack8<B>(fshr(wa, wb, off), wb >> off, P);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) P[i] = hmul2(P[i], s2);
+  return natural_order(P);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* bar_area = smem + kStages * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
+  uint64_t* bready = full + kStages;
+  uint64_t* empty = bready + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  StageMeta* meta = reinterpret_cast<StageMeta*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * BM;
+  const int k_tiles = a.K / BK;
+  const int ncols = min(BN, a.N - n0);  // valid columns of this tile (multiple of 128)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&bready[s]), kDequantWarps);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(accum), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+      int issued = 0;
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % kStages;
+        const uint32_t ph = (kt / kStages) & 1;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;
+        uint8_t* st = smem + s * kStageBytes;
+        const uint32_t bar = smem_u32(&full[s]);
+        int rows0, rows1;
+        size_t row_start;
+        if constexpr (FMT == EXQ_FMT_GPTQ4) {
+          rows0 = rows1 = 4;
+          row_start = static_cast<size_t>(kt) * 8;
+        } else {
+          const unsigned o0 = __ldg(a.seg_off + 2 * kt), o1 = __ldg(a.seg_off + 2 * kt + 1),
+                         o2 = __ldg(a.seg_off + 2 * kt + 2);
+          rows0 = static_cast<int>(o1 - o0);
+          rows1 = static_cast<int>(o2 - o1);
+          if (!valid_width(rows0) || !valid_width(rows1) || o2 > static_cast<unsigned>(a.n_word_rows) ||
+              o1 < o0) {
+            atomicOr(&g_gemm_err, kDevErrBadSegment);
+            rows0 = rows1 = 0;
+          }
+          row_start = o0;
+        }
+        meta[s].rows0 = rows0;
+        meta[s].rows1 = rows1;
+        const int rows = rows0 + rows1;
+        const uint32_t row_bytes = static_cast<uint32_t>(ncols) * 4u;
+        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * row_bytes + 2u * ncols * 2u;
+        if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (ncols / 8) * 4u;
+        mbar_expect_tx(bar, tx);
+        tma_load_2d(smem_u32(st + kOffX), &xmap, kt * BK, m0, bar);
+        for (int r = 0; r < rows; ++r)
+          bulk_load(smem_u32(st + kOffPacked + r * BN * 4), a.qweight + (row_start + r) * a.N + n0, row_bytes, bar);
+        for (int h = 0; h < 2; ++h) {
+          const int g = FMT == EXQ_FMT_GPTQ4 ? (kt * BK + 32 * h) / a.gs : 2 * kt + h;
+          bulk_load(smem_u32(st + kOffScale + h * BN * 2), a.scales + static_cast<size_t>(g) * a.N + n0,
+                    static_cast<uint32_t>(ncols) * 2u, bar);
+          if constexpr (FMT == EXQ_FMT_GPTQ4)
+            bulk_load(smem_u32(st + kOffZero + h * (BN / 8) * 4),
+                      a.qzeros + static_cast<size_t>(g) * (a.N / 8) + n0 / 8, static_cast<uint32_t>(ncols / 8) * 4u,
+                      bar);
+        }
+        issued = kt + 1;
+      }
+      // drain: every issued stage's copies must land before the CTA may exit
+      for (int kt = max(0, issued - kStages); kt < issued; ++kt) {
+        const uint32_t bar = smem_u32(&full[kt % kStages]);
+        for (long long i = 0; i < kWaitLimit; ++i)
+          if (mbar_try_wait(bar, (kt / kStages) & 1)) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % kStages;
+        const uint32_t ph = (kt / kStages) & 1;
+        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&bready[s]), ph, abort_flag)) break;
+        tc_fence_after();
+        uint8_t* st = smem + s * kStageBytes;
+        const uint64_t adesc = sw128_desc(smem_u32(st + kOffX));
+        const uint64_t bdesc = sw128_desc(smem_u32(st + kOffB));
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K inside the swizzle atom = +2 encoded
+          umma_f16(tmem, adesc + 2 * k, bdesc + 2 * k, (kt | k) != 0);
+        umma_commit(smem_u32(&empty[s]));
+      }
+      umma_commit(smem_u32(accum));
+    }
+  } else {
+    // ------------------------------------------------------------ dequantisers
+    const int dw = warp - 2;
+    const int col = dw * 32 + lane;  // output column of this thread inside the tile
+    for (int kt = 0; kt < k_tiles; ++kt) {
+      const int s = kt % kStages;
+      const uint32_t ph = (kt / kStages) & 1;
+      if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort_flag)) break;
+      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;  // B buffer consumed
+      uint8_t* st = smem + s * kStageBytes;
+      const uint32_t* packed = reinterpret_cast<const uint32_t*>(st + kOffPacked);
+      const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
+      uint8_t* btile = st + kOffB + (col >> 3) * 1024 + (col & 7) * 128;
+      const int sw = col & 7;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t s16 = sc[h * BN + col];
+        const uint32_t s2 = s16 | (s16 << 16);
+        if constexpr (FMT == EXQ_FMT_GPTQ4) {
+          const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero)[h * (BN / 8) + (col >> 3)];
+          uint32_t zlo, zhi;
+          gptq_zero_consts((zw >> (4 * (col & 7))) & 0xFu, zlo, zhi);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint32_t P[4];
+            unpack8_gptq(packed[(4 * h + t) * BN + col], zlo, zhi, P);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) P[i] = hmul2(P[i], s2);
+            const int c = 4 * h + t;  // 16-byte chunk along K
+            *reinterpret_cast<uint4*>(btile + ((c ^ sw) << 4)) = natural_order(P);
+          }
+        } else {
+          const int b = h == 0 ? meta[s].rows0 : meta[s].rows1;
+          const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint4 v;
+            switch (b) {
+              case 2: v = exl2_block<2>(rows, t, col, s2); break;
+              case 3: v = exl2_block<3>(rows, t, col, s2); break;
+              case 4: v = exl2_block<4>(rows, t, col, s2); break;
+              case 5: v = exl2_block<5>(rows, t, col, s2); break;
+              case 6: v = exl2_block<6>(rows, t, col, s2); break;
+              case 8: v = exl2_block<8>(rows, t, col, s2); break;
+              default: v = make_uint4(0, 0, 0, 0);
+            }
+            const int c = 4 * h + t;
+            *reinterpret_cast<uint4*>(btile + ((c ^ sw) << 4)) = v;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bready[s]));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (mbar_wait_warp(smem_u32(accum), 0, abort_flag)) {
+      tc_fence_after();
+      const int quarter = warp & 3;          // TMEM lanes this warp may read
+      const int half = dw >> 2;              // which 128 columns
+      const int m = m0 + quarter * 32 + lane;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c0 = half * 128 + cc * 32;
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c0, r);
+        if (m < a.M && c0 < ncols) {
+          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(m) * a.N + n0 + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 0]))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 1])))) << 16);
+            o.y = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 2]))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 3])))) << 16);
+            o.z = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 4]))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 5])))) << 16);
+            o.w = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 6]))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 7])))) << 16);
+            dst[q] = o;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// x_perm[m][j] = x[m][perm[j]]: act-order rows gathered once so the tensor map
+// reads activations in stored-row order
+__global__ void permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                 uint16_t* __restrict__ xp, int M, int K) {
+  const int chunks = K / 8;
+  const long long total = static_cast<long long>(M) * chunks;
+  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(e / chunks), c = static_cast<int>(e % chunks);
+    const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c));
+    const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c + 4));
+    const uint16_t* xr = x + static_cast<size_t>(m) * K;
+    uint4 o;
+    o.x = __ldg(xr + p0.x) | (static_cast<uint32_t>(__ldg(xr + p0.y)) << 16);
+    o.y = __ldg(xr + p0.z) | (static_cast<uint32_t>(__ldg(xr + p0.w)) << 16);
+    o.z = __ldg(xr + p1.x) | (static_cast<uint32_t>(__ldg(xr + p1.y)) << 16);
+    o.w = __ldg(xr + p1.z) | (static_cast<uint32_t>(__ldg(xr + p1.w)) << 16);
+    *reinterpret_cast<uint4*>(xp + static_cast<size_t>(m) * K + 8 * c) = o;
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
 }  // namespace
 
 size_t gemm_workspace_bytes(const exq_weight& w, int M) {
   return w.perm ? static_cast<size_t>(M) * w.K * 2 : 0;
 }
 
-exq_status launch_gemm(const exq_weight&, const uint16_t*, int, uint16_t*, void*, size_t, cudaStream_t) {
-  return EXQ_ERR_UNSUPPORTED;
+exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace, size_t,
+                       cudaStream_t stream) {
+  if (w.K % BK || w.N % 128) return EXQ_ERR_UNSUPPORTED;
+  EncodeTiled enc = encode_fn();
+  if (!enc) return EXQ_ERR_CUDA;
+
+  const uint16_t* xa = x;
+  if (w.perm) {
+    uint16_t* xp = static_cast<uint16_t*>(workspace);
+    const long long total = static_cast<long long>(M) * (w.K / 8);
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4096));
+    permute_x_kernel<<<blocks, 256, 0, stream>>>(x, w.perm, xp, M, w.K);
+    if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
+    xa = xp;
+  }
+
+  CUtensorMap xmap;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, estride,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return EXQ_ERR_CUDA;
+
+  GemmArgs args{};
+  args.qweight = w.qweight;
+  args.scales = w.scales;
+  args.qzeros = w.qzeros;
+  args.seg_off = w.seg_word_off;
+  args.y = y;
+  args.M = M;
+  args.N = w.N;
+  args.K = w.K;
+  args.gs = w.group_size;
+  args.n_word_rows = w.n_word_rows;
+  args.fmt = w.format;
+
+  auto fn = w.format == EXQ_FMT_GPTQ4 ? gemm_kernel<EXQ_FMT_GPTQ4> : gemm_kernel<EXQ_FMT_EXL2>;
+  static std::once_flag attr_once[2];
+  std::call_once(attr_once[w.format == EXQ_FMT_GPTQ4 ? 0 : 1],
+                 [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
+  const dim3 grid((w.N + BN - 1) / BN, (M + BM - 1) / BM, 1);
+  fn<<<grid, kThreads, kSmemBytes, stream>>>(xmap, args);
+  if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
+  return EXQ_OK;
 }
 
 unsigned take_gemm_errors(cudaStream_t stream) {

@@ -158,6 +158,29 @@ size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M);
 exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* exq_gemm_noalloc -- exq_gemm for callers that cannot allocate device memory.
+ * The ExLlamaV2 pages have no counterpart; this is a deployment variant.
+ * Some callers cannot hand the library a workspace: inference-runtime plugins
+ * whose enqueue path must not allocate because the host framework plans all
+ * device memory up front, and serving loops that cannot afford cudaMalloc's
+ * implicit device-wide synchronisation. For them this call takes the gathered
+ * activations of an act-order layer from a scratch array that the library
+ * reserves statically: EXQ_NOALLOC_SCRATCH_BYTES on every GPU that loads
+ * libexq, kept until the process exits. Layers without a permutation need no
+ * scratch at all.
+ *   Same arguments and results as exq_gemm without the workspace.
+ *   Returns EXQ_ERR_UNSUPPORTED (and launches nothing) if the layer has a
+ *   permutation and M * K * 2 > EXQ_NOALLOC_SCRATCH_BYTES.
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture. Nothing is allocated, then or later.
+ *   Every call on a device shares the one array, which keeps the previous
+ *   call's contents (the array is fully rewritten before it is read, so
+ *   nothing needs clearing). Calls whose kernels overlap on the GPU (other
+ *   streams, other host threads) race on it: order them on one stream. */
+#define EXQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+exq_status exq_gemm_noalloc(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Static, NUL-terminated description of a status code. */

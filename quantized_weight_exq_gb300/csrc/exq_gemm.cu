@@ -524,6 +524,44 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   return EXQ_OK;
 }
 
+namespace {
+
+// Scratch of exq_gemm_noalloc: the gathered activations of an act-order
+// layer, for callers that cannot pass a workspace. Reserved statically, so
+// every GPU that loads the library holds it until the process exits.
+__device__ __align__(256) uint8_t g_noalloc_scratch[EXQ_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on `dev`, looked up once per device
+// with that device current (in host code the symbol is only a host-side
+// stand-in, never a device address). nullptr if the lookup failed.
+void* noalloc_scratch(int dev) {
+  constexpr int kMaxDevices = 64;
+  static void* ptr[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(once[dev], [dev] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) ptr[dev] = p;
+    else cudaGetLastError();
+  });
+  return ptr[dev];
+}
+
+}  // namespace
+
+exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream) {
+  const size_t need = gemm_workspace_bytes(w, M);
+  if (need > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (need) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
+    scratch = noalloc_scratch(dev);
+    if (!scratch) return EXQ_ERR_CUDA;
+  }
+  return launch_gemm(w, x, M, y, scratch, need, stream);
+}
+
 unsigned take_gemm_errors(cudaStream_t stream) {
   unsigned v = 0, zero = 0;
   if (cudaMemcpyFromSymbolAsync(&v, g_gemm_err, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)

@@ -29,8 +29,12 @@ EXQ_FMT_EXL2 = 2
 # every symbol include/exq.h declares
 EXPORTED = (
     "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv",
-    "exq_gemm_workspace_size", "exq_gemm", "exq_status_string", "exq_get_last_device_error",
+    "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
+    "exq_get_last_device_error",
 )
+
+# size of the static scratch array exq_gemm_noalloc uses (EXQ_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class ExqError(RuntimeError):
@@ -63,6 +67,7 @@ def _load():
         "exq_gemv": (st, [W, P, i32, P, P]),
         "exq_gemm_workspace_size": (sz, [W, i32]),
         "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
+        "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
         "exq_status_string": (ctypes.c_char_p, [st]),
         "exq_get_last_device_error": (st, [P]),
     }
@@ -222,6 +227,16 @@ def exq_gemm(w: Weight, x, y, workspace=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.exq_gemm(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), ws_ptr, ws_bytes,
                          _stream_ptr(stream)), "exq_gemm")
+    return y
+
+
+def exq_gemm_noalloc(w: Weight, x, y, stream=None):
+    """exq_gemm for callers that cannot allocate: an act-order layer's
+    gathered activations go to the library's static scratch array (see
+    include/exq.h for the size limit, the first-call set-up and the rule that
+    overlapping calls race on the shared array)."""
+    _check(_lib.exq_gemm_noalloc(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(),
+                                 _stream_ptr(stream)), "exq_gemm_noalloc")
     return y
 
 

@@ -185,17 +185,22 @@ def run_exq(args, rank, world, device):
     lins, x_all, y_all = build_stream(exq, torch, args.layers, device)
     bytes_per_step = sum(w.packed_bytes for w, _, _ in lins)
     n_launch = len(lins)
+    # kernels per step: the GEMV, plus the act-order gather of x for a permuted layer
+    n_kernels = sum(2 if w.perm is not None else 1 for w, _, _ in lins)
+    # one zero-filled workspace for the whole stream, sized for its largest call
+    ws = torch.zeros(max(exq.exq_gemv_workspace_size(w, 1) for w, _, _ in lins[:len(LINEARS)]),
+                     dtype=torch.uint8, device=device)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=device)
     with torch.cuda.stream(stream):
         for w, x, y in lins[:len(LINEARS)]:      # settle per-kernel attributes before capture
-            exq.exq_gemv(w, x, y)
+            exq.exq_gemv(w, x, y, workspace=ws)
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for w, x, y in lins:
-                exq.exq_gemv(w, x, y)
+                exq.exq_gemv(w, x, y, workspace=ws)
     torch.cuda.synchronize()
     if exq.exq_get_last_device_error() != 0:
         raise RuntimeError("device error word set after warm-up")
@@ -296,7 +301,7 @@ def run_exq(args, rank, world, device):
             "frac": round(per_gpu / peak, 4),
             "traffic": None if traffic_ratio is None else round(traffic_ratio * bytes_per_launch),
             "algorithmic_bytes_per_launch": round(bytes_per_launch),
-            "kernel": "gemv_kernel<EXL2, M<=8, act-order>",
+            "kernel": "gemv_kernel<EXL2, M<=8> (+ gather_x_kernel per act-order call)",
         },
         "e2e": {
             "value": round(e2e_gbs, 2),
@@ -304,7 +309,7 @@ def run_exq(args, rank, world, device):
             "h2d_bytes_per_step": x_all.numel() * 2,
             "d2h_bytes_per_step": y_all.numel() * 2,
         },
-        "gpu_launches": n_launch * args.steps,
+        "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
     return result

@@ -134,14 +134,29 @@ int64_t exq_exl2_word_rows(const uint8_t* bits, int32_t n_segments);
  *   W_out  device fp16 [K, N], caller-allocated, fully overwritten */
 exq_status exq_dequant(const exq_weight* w, uint16_t* W_out, void* stream);
 
+/* Bytes of device workspace exq_gemv needs for this layer and M on the
+ * current device (it depends on the SM count); 0 for an invalid layer or M
+ * outside 1..16. */
+size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M);
+
 /* exq_gemv -- decode-sized fused matmul, 1 <= M <= 16 (ExLlamaV2 blog post,
  * "How the Fused CUDA Kernel Works": the packed weights are read once,
  * dequantized in registers and multiplied into fp32 sums).
  *   x  device fp16 [M, K] row-major, input-feature order
  *   y  device fp16 [M, N] row-major, fully overwritten
- * Needs no workspace. Deterministic: the same inputs give the same bits.
- * Returns EXQ_ERR_UNSUPPORTED for M > 16 (use exq_gemm). */
-exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
+ *   workspace  device buffer of at least exq_gemv_workspace_size() bytes,
+ *              256-byte aligned. Its first 64 KB hold per-tile counters of
+ *              the split over SMs: ZERO-FILL them before the first use; every
+ *              call that completes leaves them zero again, so one workspace
+ *              serves any sequence of calls (any layer, any M) ordered on one
+ *              stream. The rest is scratch (partial sums and, for a permuted
+ *              layer, x gathered into stored-row order). Calls that may
+ *              overlap on the GPU need separate workspaces.
+ * Deterministic: the same inputs give the same bits.
+ * Returns EXQ_ERR_UNSUPPORTED for M > 16 (use exq_gemm) and
+ * EXQ_ERR_INVALID_ARG for a missing, short or misaligned workspace. */
+exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
+                    void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of device workspace exq_gemm needs for this layer and M (0 if none;
  * a permuted layer needs M * K * 2 bytes for the gathered activations). */
@@ -188,7 +203,8 @@ const char* exq_status_string(exq_status s);
 
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: EXQ_OK, EXQ_ERR_TIMEOUT (a kernel gave up waiting) or
- * EXQ_ERR_INVALID_ARG (a kernel met an EXL2 segment width outside the set).
+ * EXQ_ERR_INVALID_ARG (a kernel met an EXL2 segment width outside the set or
+ * past the end of qweight, or a permutation entry outside [0, K)).
  * Returns EXQ_ERR_CUDA if the synchronisation itself fails. */
 exq_status exq_get_last_device_error(void* stream);
 

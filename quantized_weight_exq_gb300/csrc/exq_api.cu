@@ -68,13 +68,19 @@ extern "C" exq_status exq_dequant(const exq_weight* w, uint16_t* W_out, void* st
   return launch_dequant(*w, W_out, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream) {
+extern "C" size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M) {
+  if (check_weight(w) != EXQ_OK || M < 1 || M > 16) return 0;
+  return gemv_workspace_bytes(*w, M);
+}
+
+extern "C" exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
+                               size_t ws_bytes, void* stream) {
   const exq_status st = check_weight(w);
   if (st != EXQ_OK) return st;
   if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
   if (M > 16) return EXQ_ERR_UNSUPPORTED;
   if (current_cc() < 100) return EXQ_ERR_CUDA;
-  return launch_gemv(*w, x, M, y, static_cast<cudaStream_t>(stream));
+  return launch_gemv(*w, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M) {
@@ -120,6 +126,6 @@ extern "C" exq_status exq_get_last_device_error(void* stream) {
   if (a == ~0u || b == ~0u || c == ~0u) return EXQ_ERR_CUDA;
   const unsigned v = a | b | c;
   if (v & kDevErrTimeout) return EXQ_ERR_TIMEOUT;
-  if (v & kDevErrBadSegment) return EXQ_ERR_INVALID_ARG;
+  if (v & (kDevErrBadSegment | kDevErrBadPerm)) return EXQ_ERR_INVALID_ARG;
   return EXQ_OK;
 }

@@ -12,6 +12,7 @@ namespace exq {
 enum : unsigned {
   kDevErrTimeout = 1u,      // a bounded wait gave up
   kDevErrBadSegment = 2u,   // an EXL2 segment width outside {2,3,4,5,6,8} or past the end
+  kDevErrBadPerm = 4u,      // a permutation entry outside [0, K)
 };
 
 struct DeviceInfo {
@@ -23,7 +24,9 @@ struct DeviceInfo {
 // queried once per device, cached (host-only, thread-safe)
 const DeviceInfo& device_info(int device);
 
-exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream);
+exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+size_t gemv_workspace_bytes(const exq_weight& w, int M);
 exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t stream);
 exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);

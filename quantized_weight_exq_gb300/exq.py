@@ -28,8 +28,8 @@ EXQ_FMT_EXL2 = 2
 
 # every symbol include/exq.h declares
 EXPORTED = (
-    "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv",
-    "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
+    "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
+    "exq_gemv", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error",
 )
 
@@ -64,7 +64,8 @@ def _load():
         "exq_pack_exl2": (st, [P, P, i32, i32, P, P]),
         "exq_exl2_word_rows": (i64, [P, i32]),
         "exq_dequant": (st, [W, P, P]),
-        "exq_gemv": (st, [W, P, i32, P, P]),
+        "exq_gemv_workspace_size": (sz, [W, i32]),
+        "exq_gemv": (st, [W, P, i32, P, P, sz, P]),
         "exq_gemm_workspace_size": (sz, [W, i32]),
         "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
         "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
@@ -212,9 +213,34 @@ def exq_dequant(w: Weight, W_out, stream=None):
     return W_out
 
 
-def exq_gemv(w: Weight, x, y, stream=None):
-    _check(_lib.exq_gemv(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), _stream_ptr(stream)),
-           "exq_gemv")
+def exq_gemv_workspace_size(w: Weight, M: int) -> int:
+    return int(_lib.exq_gemv_workspace_size(ctypes.byref(w.desc()), M))
+
+
+_gemv_ws = {}  # device index -> zero-filled uint8 workspace shared by calls on one stream
+
+
+def gemv_workspace(w: Weight, M: int):
+    """A zero-filled exq_gemv workspace for the current device, kept and grown
+    across calls. exq_gemv leaves it zeroed, so calls ordered on one stream can
+    share it; calls that may overlap on the GPU need their own (torch.zeros of
+    exq_gemv_workspace_size bytes)."""
+    import torch
+    need = exq_gemv_workspace_size(w, M)
+    dev = torch.cuda.current_device()
+    buf = _gemv_ws.get(dev)
+    if buf is None or buf.numel() < need:
+        buf = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=f"cuda:{dev}")
+        _gemv_ws[dev] = buf
+    return buf
+
+
+def exq_gemv(w: Weight, x, y, workspace=None, stream=None):
+    if workspace is None:
+        workspace = gemv_workspace(w, x.shape[0])
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.exq_gemv(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), workspace.data_ptr(),
+                         ws_bytes, _stream_ptr(stream)), "exq_gemv")
     return y
 
 

@@ -100,14 +100,18 @@ def test_device_entry_points_validate_on_host(exq):
     ]
     for kw in bad:
         d = _desc(exq, **kw)
-        assert lib.exq_gemv(ctypes.byref(d), 0x50000, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG, kw
+        assert lib.exq_gemv(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
         assert lib.exq_dequant(ctypes.byref(d), 0x60000, None) == exq.EXQ_ERR_INVALID_ARG, kw
         assert lib.exq_gemm(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
     d = _desc(exq)
-    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 17, 0x60000, None) == exq.EXQ_ERR_UNSUPPORTED
-    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 0, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
-    assert lib.exq_gemv(ctypes.byref(d), 0x50008, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
-    assert lib.exq_gemv(None, 0x50000, 1, 0x60000, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 17, 0x60000, None, 0, None) == exq.EXQ_ERR_UNSUPPORTED
+    assert lib.exq_gemv(ctypes.byref(d), 0x50000, 0, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_gemv(ctypes.byref(d), 0x50008, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_gemv(None, 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+    # the decode workspace size is 0 outside M = 1..16 and for a bad layer
+    assert lib.exq_gemv_workspace_size(ctypes.byref(d), 17) == 0
+    assert lib.exq_gemv_workspace_size(ctypes.byref(d), 0) == 0
+    assert lib.exq_gemv_workspace_size(ctypes.byref(_desc(exq, N=60)), 1) == 0
     # act-order prefill needs a workspace for the gathered activations
     dp = _desc(exq, perm=0x70000)
     assert lib.exq_gemm_workspace_size(ctypes.byref(dp), 128) == 128 * 256 * 2

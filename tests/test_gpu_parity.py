@@ -167,6 +167,52 @@ def test_device_error_word_bad_segment(env):
     assert exq.exq_get_last_device_error() == 0  # read-and-clear
 
 
+@pytest.mark.parametrize("ctas", [1, 2, 5, 37, 1000])
+def test_gemv_any_split_over_ctas(env, ctas, monkeypatch):
+    # the (tile, step) work is shared evenly by however many CTAs run; tiles
+    # split between CTAs meet in the workspace. Every split gives the oracle's
+    # result, and every call leaves the workspace counters at zero.
+    exq, torch = env
+    monkeypatch.setenv("EXQ_GEMV_CTAS", str(ctas))
+    g = gptq_case(2048, 264, 64, act_order=True, seed=ctas)
+    e = exl2_case(2048, 200, bpw=4.0, permute=True, seed=ctas)
+    for w, W_ref in ((_gptq_dev(exq, g), oracle_W_gptq(g)), (_exl2_dev(exq, e), oracle_W_exl2(e))):
+        for M in (1, 9):
+            x = synth.activations(M, w.K, seed=M + ctas)
+            ws = torch.zeros(exq.exq_gemv_workspace_size(w, M), dtype=torch.uint8, device="cuda")
+            y = torch.full((M, w.N), float("nan"), dtype=torch.float16, device="cuda")
+            exq.exq_gemv(w, _x(torch, x), y, workspace=ws)
+            torch.cuda.synchronize()
+            assert exq.exq_get_last_device_error() == 0
+            assert int(ws[:65536].view(torch.int32).abs().sum()) == 0  # the counters are zero again
+            check_matmul(y.float().cpu().numpy().astype(np.float64), O.matmul(x, W_ref), f"ctas={ctas} M={M}")
+
+
+def test_gemv_workspace_contract(env):
+    exq, torch = env
+    e = exl2_case(1024, 128, seed=11)
+    w = _exl2_dev(exq, e)
+    need = exq.exq_gemv_workspace_size(w, 1)
+    assert need > 0
+    x = _x(torch, synth.activations(1, 1024, seed=1))
+    y = torch.empty(1, 128, dtype=torch.float16, device="cuda")
+    short = torch.zeros(need - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(exq.ExqError) as ei:
+        exq.exq_gemv(w, x, y, workspace=short)
+    assert ei.value.status == exq.EXQ_ERR_INVALID_ARG
+    # one workspace serves a run of calls with different layers and M
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+    for K, N, M in ((1024, 128, 1), (4096, 1024, 16), (2048, 264, 3)):
+        ee = exl2_case(K, N, seed=K + M)
+        ww = _exl2_dev(exq, ee)
+        xx = synth.activations(M, K, seed=M)
+        yy = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        exq.exq_gemv(ww, _x(torch, xx), yy, workspace=ws)
+        torch.cuda.synchronize()
+        check_matmul(yy.float().cpu().numpy().astype(np.float64), O.matmul(xx, oracle_W_exl2(ee)), f"ws K={K} M={M}")
+    assert int(ws[:65536].view(torch.int32).abs().sum()) == 0  # the counter region is zero again
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def _sample_cols(N, n=256, seed=0):

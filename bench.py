@@ -174,6 +174,24 @@ def build_stream(exq, torch, layers: int, device):
     return lin_list, x_all, y_all
 
 
+def max_over_ranks(times, world, device=None):
+    """The slowest rank's times: every rank waits for all of them (all-reduce
+    MAX over the process group; a CPU tensor under gloo)."""
+    if world <= 1:
+        return list(times)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(times), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_throughput(bytes_per_step: int, steps: int, t_ms: float, world: int) -> float:
+    """Whole-job GB/s: every replica streams bytes_per_step per step, and the
+    job takes the slowest rank's time."""
+    return world * bytes_per_step * steps / (t_ms * 1e-3) / 1e9
+
+
 def run_exq(args, rank, world, device):
     import torch
 
@@ -250,17 +268,13 @@ def run_exq(args, rank, world, device):
     torch.cuda.synchronize()
     t_e2e_ms = timed(e2e_step, args.steps)
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_ms, t_e2e_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms, t_e2e_ms = float(t[0]), float(t[1])
+    t_ms, t_e2e_ms = max_over_ranks([t_ms, t_e2e_ms], world, device)
 
     if exq.exq_get_last_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
-    gbs = world * bytes_per_step * args.steps / (t_ms * 1e-3) / 1e9
-    e2e_gbs = world * bytes_per_step * args.steps / (t_e2e_ms * 1e-3) / 1e9
+    gbs = job_throughput(bytes_per_step, args.steps, t_ms, world)
+    e2e_gbs = job_throughput(bytes_per_step, args.steps, t_e2e_ms, world)
     peak, peak_kind = measured_peaks()
     per_gpu = gbs / world
     traffic_ratio = profile_traffic()

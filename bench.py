@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--impl", default="exq", choices=["exq", "reference"])
     ap.add_argument("--layers", type=int, default=80, help="decoder layers in the stream (80 = Llama-2-70B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the prefill GEMM over the 70B shapes instead (one JSON line, TFLOPS per shape)")
     return ap.parse_args()
 
 
@@ -172,6 +174,86 @@ def build_stream(exq, torch, layers: int, device):
             yo += N
             lin_list.append((w, x, y))
     return lin_list, x_all, y_all
+
+
+PREFILL_SHAPES = (("q", 8192, 8192), ("k", 8192, 1024), ("gate", 8192, 28672), ("down", 28672, 8192))
+
+
+def run_prefill(args, device):
+    """The prefill GEMM over the Llama-2-70B projection shapes at M = 512 and
+    2048, GPTQ g128 (no act-order) and EXL2 2.5 bpw from {2, 3, 4}; packed
+    words drawn uniformly on the device (the packing is a bijection, so this is
+    the distribution of uniform codes). CUDA events around `--steps` launches
+    after `--warmup`; TFLOPS = 2 M K N / time."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    peak_bf16 = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_bf16 = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        peak_bf16 = 1900.0
+    shapes = {}
+    for fmt in ("gptq_g128", "exl2_2.5bpw"):
+        for M in (512, 2048):
+            for name, K, N in PREFILL_SHAPES:
+                gen = torch.Generator(device=device)
+                gen.manual_seed(1000 * M + K + N)
+                if fmt.startswith("gptq"):
+                    qw = torch.randint(0, 2 ** 32, (K // 8, N), dtype=torch.int64, device=device,
+                                       generator=gen).to(torch.int32)
+                    qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
+                                       generator=gen).to(torch.int32)
+                    sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
+                    w = exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device)
+                else:
+                    bits = synth.solve_bit_mix(K // 32, 2.5, (2, 3, 4), np.random.default_rng(K + N))
+                    off = np.zeros(bits.size + 1, np.int64)
+                    off[1:] = np.cumsum(bits)
+                    qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device,
+                                       generator=gen).to(torch.int32)
+                    sc = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
+                    w = exq.exl2_weight(qw, off.astype(np.int32), sc, None, K, N, device=device)
+                x = torch.randn(M, K, device=device, generator=gen).half()
+                y = torch.empty(M, N, device=device, dtype=torch.float16)
+                nws = exq.exq_gemm_workspace_size(w, M)
+                ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device) if nws else None
+                for _ in range(args.warmup):
+                    exq.exq_gemm(w, x, y, ws)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    exq.exq_gemm(w, x, y, ws)
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1000 / args.steps
+                tf = 2 * M * K * N / us / 1e6
+                shapes[f"{fmt} M={M} {name} {K}x{N}"] = {"us": round(us, 1), "tflops": round(tf, 1),
+                                                          "frac": round(tf / peak_bf16, 4)}
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the prefill sweep")
+    best = max(v["tflops"] for v in shapes.values())
+    return {
+        "metric": "prefill GEMM TFLOPS (fp16 in, fp32 accumulate)",
+        "value": best,
+        "unit": "TFLOPS",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "prefill_70b_shapes", "value_is": "best shape"},
+        "roofline": {"bound": "tensor", "peak": peak_bf16, "unit": "TFLOPS",
+                     "peak_kind": "measured bf16 cuBLAS burst (fp16 runs at the same rate)"},
+        "shapes": shapes,
+    }
 
 
 def max_over_ranks(times, world, device=None):
@@ -418,6 +500,10 @@ def main():
         return
 
     import torch
+    if args.prefill:
+        if rank == 0:
+            print(json.dumps(run_prefill(args, torch.device("cuda", local))), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)

@@ -5,20 +5,23 @@
 // quantized Llama/HF models", section "How the Fused CUDA Kernel Works")
 // describes the fused kernel as loading packed weights, dequantising on the
 // fly and doing the matmul in the same kernel without an intermediate write,
-// "using tensor cores". Here that becomes, per 128 x 256 output tile:
+// "using tensor cores". Here that becomes, per 256 x 128 output tile:
 //
-//   warp 0      TMA producer: the x tile (128 x 64 fp16, 128-byte swizzle)
-//               through a tensor map, and the packed word rows, scales and
-//               zeros of the 64-row K slab as 1-D bulk copies (EXL2 segments
-//               have data-dependent row counts, which fixed TMA boxes cannot
-//               express), all completing on one mbarrier per stage.
+//   warp 0      TMA producer: the x tile (128 x 64 fp16, 128-byte swizzle),
+//               the packed word rows of the 64-row K slab (one tensor-map box
+//               of 8 rows x 256 columns for GPTQ; one box per 32-row EXL2
+//               segment, of exactly its width, from a tensor map per width),
+//               its scale rows and GPTQ zero rows, all completing on one
+//               mbarrier per stage.
 //   warps 2-9   dequantisers: packed words -> exact fp16 (q - z) -> * s, one
-//               output column per thread, written to shared memory as the
-//               K-major, 128-byte-swizzled B operand; then the epilogue.
+//               column and 32-row half per thread, written to shared memory
+//               as the K-major, 128-byte-swizzled B operand; then the epilogue.
 //   warp 1      allocates tensor memory; one elected lane issues
-//               tcgen05.mma.kind::f16 (M=128, N=256, K=16) x 4 per stage,
-//               accumulating fp32 in TMEM, and commits each stage back to its
-//               "empty" mbarrier.
+//               tcgen05.mma.kind::f16 (M=128, N=128, K=16) x 4 per stage for
+//               each of the tile's two 128-row halves, against the same B
+//               stage (one dequantisation serves 256 rows of x), accumulating
+//               fp32 in TMEM, and commits each stage back to its "empty"
+//               mbarrier.
 //   epilogue    tcgen05.ld 32x32b -> fp16 -> global.
 //
 // Act-order (a stored-row permutation) is applied to x by a gather kernel
@@ -28,6 +31,7 @@
 #include <cuda.h>
 
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "exq_device.cuh"
@@ -38,17 +42,19 @@ namespace {
 
 __device__ unsigned g_gemm_err;
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 256, BN = 128, BK = 64;  // CTA tile
+constexpr int UM = 128;                       // rows per MMA: two accumulators share each B stage
 constexpr int kStages = 3;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = (2 + kDequantWarps) * 32;
 
 // per-stage shared memory layout (bytes)
-constexpr int kXBytes = BM * BK * 2;        // 16 KB, 1024-aligned
-constexpr int kBBytes = BN * BK * 2;        // 32 KB, 1024-aligned
+constexpr int kXBytes = BM * BK * 2;        // 32 KB, 1024-aligned
+constexpr int kBBytes = BN * BK * 2;        // 16 KB, 1024-aligned
 constexpr int kPackedBytes = 16 * BN * 4;   // up to 16 word rows (two 8-bit segments)
 constexpr int kScaleBytes = 2 * BN * 2;     // two 32-row halves
-constexpr int kZeroBytes = 2 * (BN / 8) * 4;
+constexpr int kZeroStride = 128;            // each half's zero row on its own 128-byte boundary (TMA)
+constexpr int kZeroBytes = 2 * kZeroStride;
 constexpr int kOffX = 0;
 constexpr int kOffB = kOffX + kXBytes;
 constexpr int kOffPacked = kOffB + kBBytes;
@@ -57,9 +63,25 @@ constexpr int kOffZero = kOffScale + kScaleBytes;
 constexpr int kStageBytes = ((kOffZero + kZeroBytes + 1023) / 1024) * 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// every TMA destination starts on a 128-byte boundary (1024 for the swizzled x tile)
+static_assert(kOffX % 1024 == 0 && kOffB % 1024 == 0, "operand alignment");
+static_assert(kOffPacked % 128 == 0 && (BN * 4) % 128 == 0, "packed-row boxes");
+static_assert(kOffScale % 128 == 0 && (BN * 2) % 128 == 0, "scale boxes");
+static_assert(kOffZero % 128 == 0 && (BN / 8) * 4 <= kZeroStride, "zero boxes");
+static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 2 * BN;  // two 128 x BN fp32 accumulators
 constexpr long long kWaitLimit = 1ll << 22;  // try_wait rounds before giving up
+
+struct GemmMaps {
+  CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 128, 128-byte swizzle
+  CUtensorMap w[6];  // qweight [rows, N] uint32, boxes 256 columns x b rows, b in {2,3,4,5,6,8}
+  CUtensorMap s;     // scales [groups, N] fp16, boxes 256 x 1
+  CUtensorMap z;     // GPTQ zeros [groups, N / 8] uint32, boxes 32 x 1
+};
+
+// tensor map of a box of b word rows
+__device__ __forceinline__ int wmap_index(int b) { return b == 8 ? 5 : b - 2; }
 
 struct GemmArgs {
   const uint32_t* qweight;
@@ -136,12 +158,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -162,7 +178,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 
 // instruction descriptor: D fp32, A/B fp16, both K-major, M = 128, N = 256
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+                            (static_cast<uint32_t>(UM >> 4) << 24);
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
@@ -217,11 +233,21 @@ __device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col
   return natural_order(P);
 }
 
+// the 32 codes of one column of a width-B segment -> 4 swizzled 16-byte
+// chunks (c0 .. c0 + 3) of the column's K-major B-operand row
+template <int B>
+__device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint8_t* btile, int c0,
+                                             int sw) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    *reinterpret_cast<uint4*>(btile + (((c0 + t) ^ sw) << 4)) = exl2_block<B>(rows, t, col, s2);
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ GemmArgs a) {
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* bar_area = smem + kStages * kStageBytes;
@@ -263,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
       int issued = 0;
       for (int kt = 0; kt < k_tiles; ++kt) {
         const int s = kt % kStages;
@@ -272,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = smem + s * kStageBytes;
         const uint32_t bar = smem_u32(&full[s]);
         int rows0, rows1;
-        size_t row_start;
+        int row_start;
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
           rows0 = rows1 = 4;
-          row_start = static_cast<size_t>(kt) * 8;
+          row_start = kt * 8;
         } else {
           const unsigned o0 = __ldg(a.seg_off + 2 * kt), o1 = __ldg(a.seg_off + 2 * kt + 1),
                          o2 = __ldg(a.seg_off + 2 * kt + 2);
@@ -286,26 +312,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(&g_gemm_err, kDevErrBadSegment);
             rows0 = rows1 = 0;
           }
-          row_start = o0;
+          row_start = static_cast<int>(o0);
         }
         meta[s].rows0 = rows0;
         meta[s].rows1 = rows1;
         const int rows = rows0 + rows1;
-        const uint32_t row_bytes = static_cast<uint32_t>(ncols) * 4u;
-        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * row_bytes + 2u * ncols * 2u;
-        if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (ncols / 8) * 4u;
+        // boxes always move their full size (columns past N read as zero)
+        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u + 2u * BN * 2u;
+        if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (BN / 8) * 4u;
         mbar_expect_tx(bar, tx);
-        tma_load_2d(smem_u32(st + kOffX), &xmap, kt * BK, m0, bar);
-        for (int r = 0; r < rows; ++r)
-          bulk_load(smem_u32(st + kOffPacked + r * BN * 4), a.qweight + (row_start + r) * a.N + n0, row_bytes, bar);
+        tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
+        if constexpr (FMT == EXQ_FMT_GPTQ4) {
+          tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(8)], n0, row_start, bar);
+        } else if (rows > 0) {
+          tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(rows0)], n0, row_start, bar);
+          tma_load_2d(smem_u32(st + kOffPacked + rows0 * BN * 4), &maps.w[wmap_index(rows1)], n0, row_start + rows0,
+                      bar);
+        }
         for (int h = 0; h < 2; ++h) {
           const int g = FMT == EXQ_FMT_GPTQ4 ? (kt * BK + 32 * h) / a.gs : 2 * kt + h;
-          bulk_load(smem_u32(st + kOffScale + h * BN * 2), a.scales + static_cast<size_t>(g) * a.N + n0,
-                    static_cast<uint32_t>(ncols) * 2u, bar);
+          tma_load_2d(smem_u32(st + kOffScale + h * BN * 2), &maps.s, n0, g, bar);
           if constexpr (FMT == EXQ_FMT_GPTQ4)
-            bulk_load(smem_u32(st + kOffZero + h * (BN / 8) * 4),
-                      a.qzeros + static_cast<size_t>(g) * (a.N / 8) + n0 / 8, static_cast<uint32_t>(ncols / 8) * 4u,
-                      bar);
+            tma_load_2d(smem_u32(st + kOffZero + h * kZeroStride), &maps.z, n0 / 8, g, bar);
         }
         issued = kt + 1;
       }
@@ -327,10 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         uint8_t* st = smem + s * kStageBytes;
         const uint64_t adesc = sw128_desc(smem_u32(st + kOffX));
+        const uint64_t adesc1 = sw128_desc(smem_u32(st + kOffX + UM * 128));  // rows 128 .. 255
         const uint64_t bdesc = sw128_desc(smem_u32(st + kOffB));
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K inside the swizzle atom = +2 encoded
+        for (int k = 0; k < BK / 16; ++k) {  // +32 bytes along K inside the swizzle atom = +2 encoded
           umma_f16(tmem, adesc + 2 * k, bdesc + 2 * k, (kt | k) != 0);
+          umma_f16(tmem + BN, adesc1 + 2 * k, bdesc + 2 * k, (kt | k) != 0);
+        }
         umma_commit(smem_u32(&empty[s]));
       }
       umma_commit(smem_u32(accum));
@@ -338,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ dequantisers
     const int dw = warp - 2;
-    const int col = dw * 32 + lane;  // output column of this thread inside the tile
+    const int col = (dw & 3) * 32 + lane;  // output column of this thread inside the tile
+    const int h = dw >> 2;                 // its 32-row half of the 64-row K slab
     for (int kt = 0; kt < k_tiles; ++kt) {
       const int s = kt % kStages;
       const uint32_t ph = (kt / kStages) & 1;
@@ -349,12 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
       uint8_t* btile = st + kOffB + (col >> 3) * 1024 + (col & 7) * 128;
       const int sw = col & 7;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
         const uint32_t s16 = sc[h * BN + col];
         const uint32_t s2 = s16 | (s16 << 16);
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero)[h * (BN / 8) + (col >> 3)];
+          const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
           uint32_t zlo, zhi;
           gptq_zero_consts((zw >> (4 * (col & 7))) & 0xFu, zlo, zhi);
 #pragma unroll
@@ -369,20 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int b = h == 0 ? meta[s].rows0 : meta[s].rows1;
           const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
+          // one branch per 32-row segment, each width's 4 blocks unrolled inside
+          switch (b) {
+            case 2: exl2_segment<2>(rows, col, s2, btile, 4 * h, sw); break;
+            case 3: exl2_segment<3>(rows, col, s2, btile, 4 * h, sw); break;
+            case 4: exl2_segment<4>(rows, col, s2, btile, 4 * h, sw); break;
+            case 5: exl2_segment<5>(rows, col, s2, btile, 4 * h, sw); break;
+            case 6: exl2_segment<6>(rows, col, s2, btile, 4 * h, sw); break;
+            case 8: exl2_segment<8>(rows, col, s2, btile, 4 * h, sw); break;
+            default:
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint4 v;
-            switch (b) {
-              case 2: v = exl2_block<2>(rows, t, col, s2); break;
-              case 3: v = exl2_block<3>(rows, t, col, s2); break;
-              case 4: v = exl2_block<4>(rows, t, col, s2); break;
-              case 5: v = exl2_block<5>(rows, t, col, s2); break;
-              case 6: v = exl2_block<6>(rows, t, col, s2); break;
-              case 8: v = exl2_block<8>(rows, t, col, s2); break;
-              default: v = make_uint4(0, 0, 0, 0);
-            }
-            const int c = 4 * h + t;
-            *reinterpret_cast<uint4*>(btile + ((c ^ sw) << 4)) = v;
+              for (int t = 0; t < 4; ++t)
+                *reinterpret_cast<uint4*>(btile + (((4 * h + t) ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
           }
         }
       }
@@ -395,13 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (mbar_wait_warp(smem_u32(accum), 0, abort_flag)) {
       tc_fence_after();
       const int quarter = warp & 3;          // TMEM lanes this warp may read
-      const int half = dw >> 2;              // which 128 columns
-      const int m = m0 + quarter * 32 + lane;
+      const int acc = dw >> 2;               // which accumulator (rows 0..127 or 128..255)
+      const int m = m0 + acc * UM + quarter * 32 + lane;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int c0 = half * 128 + cc * 32;
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        const int c0 = cc * 32;
         uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c0, r);
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + c0, r);
         if (m < a.M && c0 < ncols) {
           uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(m) * a.N + n0 + c0);
 #pragma unroll
@@ -491,15 +520,47 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     xa = xp;
   }
 
-  CUtensorMap xmap;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
-  const cuuint32_t box[2] = {BK, BM};
-  const cuuint32_t estride[2] = {1, 1};
-  if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, estride,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return EXQ_ERR_CUDA;
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const cuuint32_t es[2] = {1, 1};
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (enc(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return EXQ_ERR_CUDA;
+  }
+  static const int kWidths[6] = {2, 3, 4, 5, 6, 8};
+  for (int i = 0; i < 6; ++i) {
+    if (w.format == EXQ_FMT_GPTQ4 && kWidths[i] != 8) continue;  // GPTQ: 8 word rows per 64-row slab
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_word_rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 4};
+    const cuuint32_t box[2] = {BN, static_cast<cuuint32_t>(kWidths[i])};
+    if (enc(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qweight), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return EXQ_ERR_CUDA;
+  }
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_groups)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 2};
+    const cuuint32_t box[2] = {BN, 1};
+    if (enc(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(w.scales), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return EXQ_ERR_CUDA;
+  }
+  if (w.format == EXQ_FMT_GPTQ4) {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N / 8), static_cast<cuuint64_t>(w.n_groups)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N / 8) * 4};
+    const cuuint32_t box[2] = {BN / 8, 1};
+    if (enc(&maps.z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qzeros), gdim, gstride, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return EXQ_ERR_CUDA;
+  }
 
   GemmArgs args{};
   args.qweight = w.qweight;
@@ -519,7 +580,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   std::call_once(attr_once[w.format == EXQ_FMT_GPTQ4 ? 0 : 1],
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
   const dim3 grid((w.N + BN - 1) / BN, (M + BM - 1) / BM, 1);
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(xmap, args);
+  fn<<<grid, kThreads, kSmemBytes, stream>>>(maps, args);
   if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
   return EXQ_OK;
 }

@@ -158,18 +158,29 @@ size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M);
 exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
                     void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of device workspace exq_gemm needs for this layer and M (0 if none;
- * a permuted layer needs M * K * 2 bytes for the gathered activations). */
+/* Bytes of device workspace exq_gemm needs for this layer and M (0 if none).
+ * Two parts, both scratch: for a permuted layer, M * K * 2 bytes (rounded up
+ * to 256) of activations gathered into stored-row order; and, when the grid
+ * of 128-column x 256-token tiles is too small to fill the GPU (fewer tiles
+ * than half the SMs), split * M * N * 4 bytes of fp32 partial sums of a K
+ * split (split <= 8, each split at least 512 rows of K). The size is the
+ * largest any device (up to 256 SMs) would use, so it does not depend on the
+ * current device. */
 size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M);
 
 /* exq_gemm -- prefill-sized fused matmul for any M >= 1 (tuned for M >= 128):
- * packed tiles are dequantized to fp16 in shared memory and fed to the
- * tcgen05 tensor cores with fp32 accumulation in tensor memory.
+ * computed as y^T = W^T x^T on the tcgen05 tensor cores, the packed weights
+ * dequantized to fp16 straight into tensor memory as the A operand, x read
+ * by TMA as the B operand, fp32 accumulation in tensor memory.
  *   x  device fp16 [M, K], y device fp16 [M, N] (fully overwritten)
  *   workspace  device buffer of at least exq_gemm_workspace_size() bytes
  *              (may be NULL when that size is 0); contents are scratch.
+ *              Calls that may overlap on the GPU need separate workspaces.
+ * With a K split a second kernel adds the splits' partial sums in split
+ * order: the same inputs give the same bits on the same device.
  * Requires K % 64 == 0 and N % 128 == 0 in addition to the rules above,
- * else EXQ_ERR_UNSUPPORTED. */
+ * else EXQ_ERR_UNSUPPORTED; a missing, short or misaligned workspace is
+ * EXQ_ERR_INVALID_ARG. */
 exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
                     void* workspace, size_t ws_bytes, void* stream);
 
@@ -183,7 +194,9 @@ exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t*
  * reserves statically: EXQ_NOALLOC_SCRATCH_BYTES on every GPU that loads
  * libexq, kept until the process exits. Layers without a permutation need no
  * scratch at all.
- *   Same arguments and results as exq_gemm without the workspace.
+ *   Same arguments and results as exq_gemm without the workspace, except
+ *   that it never splits K (the partial sums would need more scratch), so
+ *   grids of few tiles run slower and may round differently in the last bit.
  *   Returns EXQ_ERR_UNSUPPORTED (and launches nothing) if the layer has a
  *   permutation and M * K * 2 > EXQ_NOALLOC_SCRATCH_BYTES.
  *   The first call on a device looks up the scratch array's device address

@@ -104,7 +104,7 @@ extern "C" exq_status exq_gemm_noalloc(const exq_weight* w, const uint16_t* x, i
   const exq_status st = check_weight(w);
   if (st != EXQ_OK) return st;
   if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
-  if (gemm_workspace_bytes(*w, M) > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
+  if (gemm_gather_bytes(*w, M) > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
   if (current_cc() < 100) return EXQ_ERR_CUDA;
   return launch_gemm_noalloc(*w, x, M, y, static_cast<cudaStream_t>(stream));
 }

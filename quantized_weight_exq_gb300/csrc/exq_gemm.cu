@@ -5,24 +5,29 @@
 // quantized Llama/HF models", section "How the Fused CUDA Kernel Works")
 // describes the fused kernel as loading packed weights, dequantising on the
 // fly and doing the matmul in the same kernel without an intermediate write,
-// "using tensor cores". Here that becomes, per 256 x 128 output tile:
+// "using tensor cores". Here the product is computed transposed, y^T = W^T x^T,
+// so that the dequantised weights are the MMA's A operand and live in tensor
+// memory, never in shared memory. Per CTA tile of 128 output columns x 256
+// tokens and per 64-row K slab:
 //
-//   warp 0      TMA producer: the x tile (128 x 64 fp16, 128-byte swizzle),
-//               the packed word rows of the 64-row K slab (one tensor-map box
-//               of 8 rows x 256 columns for GPTQ; one box per 32-row EXL2
+//   warp 0      TMA producer: the x tile (256 tokens x 64 fp16, 128-byte
+//               swizzle), the packed word rows of the slab (one tensor-map box
+//               of 8 rows x 128 columns for GPTQ; one box per 32-row EXL2
 //               segment, of exactly its width, from a tensor map per width),
 //               its scale rows and GPTQ zero rows, all completing on one
-//               mbarrier per stage.
-//   warps 2-9   dequantisers: packed words -> exact fp16 (q - z) -> * s, one
-//               column and 32-row half per thread, written to shared memory
-//               as the K-major, 128-byte-swizzled B operand; then the epilogue.
+//               mbarrier per stage (5 stages).
+//   warps 2-9   dequantisers: thread = output column (its TMEM lane), warp
+//               pair = the slab's two 32-row halves; packed words -> exact
+//               fp16 (q - z) -> * s, stored with tcgen05.st as the K-major A
+//               operand (128 lanes x 32 columns per stage); then the epilogue.
 //   warp 1      allocates tensor memory; one elected lane issues
-//               tcgen05.mma.kind::f16 (M=128, N=128, K=16) x 4 per stage for
-//               each of the tile's two 128-row halves, against the same B
-//               stage (one dequantisation serves 256 rows of x), accumulating
-//               fp32 in TMEM, and commits each stage back to its "empty"
-//               mbarrier.
-//   epilogue    tcgen05.ld 32x32b -> fp16 -> global.
+//               tcgen05.mma.kind::f16 with A in TMEM and x (B, N = up to 256
+//               tokens) in shared memory, M = 128, K = 16, four per slab,
+//               accumulating fp32 in TMEM, and commits each stage back to its
+//               "empty" mbarrier.
+//   epilogue    tcgen05.ld 32x32b (lane = output column, column = token) ->
+//               fp16 -> global; with a K split, fp32 partial sums go to the
+//               workspace and a second kernel adds them in split order.
 //
 // Act-order (a stored-row permutation) is applied to x by a gather kernel
 // into the caller's workspace first, so the tensor map reads x in stored-row
@@ -42,36 +47,46 @@ namespace {
 
 __device__ unsigned g_gemm_err;
 
-constexpr int BM = 256, BN = 128, BK = 64;  // CTA tile
-constexpr int UM = 128;                       // rows per MMA: two accumulators share each B stage
-constexpr int kStages = 3;
+constexpr int BN = 128;   // output columns per CTA = MMA M = TMEM lanes
+constexpr int BT = 256;   // tokens per CTA = MMA N (at most)
+constexpr int BK = 64;    // K rows per stage
+constexpr int kStages = 5;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = (2 + kDequantWarps) * 32;
 
 // per-stage shared memory layout (bytes)
-constexpr int kXBytes = BM * BK * 2;        // 32 KB, 1024-aligned
-constexpr int kBBytes = BN * BK * 2;        // 16 KB, 1024-aligned
+constexpr int kXBytes = BT * BK * 2;        // 32 KB, 1024-aligned
 constexpr int kPackedBytes = 16 * BN * 4;   // up to 16 word rows (two 8-bit segments)
 constexpr int kScaleBytes = 2 * BN * 2;     // two 32-row halves
 constexpr int kZeroStride = 128;            // each half's zero row on its own 128-byte boundary (TMA)
 constexpr int kZeroBytes = 2 * kZeroStride;
 constexpr int kOffX = 0;
-constexpr int kOffB = kOffX + kXBytes;
-constexpr int kOffPacked = kOffB + kBBytes;
+constexpr int kOffPacked = kOffX + kXBytes;
 constexpr int kOffScale = kOffPacked + kPackedBytes;
 constexpr int kOffZero = kOffScale + kScaleBytes;
 constexpr int kStageBytes = ((kOffZero + kZeroBytes + 1023) / 1024) * 1024;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 // every TMA destination starts on a 128-byte boundary (1024 for the swizzled x tile)
-static_assert(kOffX % 1024 == 0 && kOffB % 1024 == 0, "operand alignment");
+static_assert(kOffX % 1024 == 0, "operand alignment");
 static_assert(kOffPacked % 128 == 0 && (BN * 4) % 128 == 0, "packed-row boxes");
 static_assert(kOffScale % 128 == 0 && (BN * 2) % 128 == 0, "scale boxes");
 static_assert(kOffZero % 128 == 0 && (BN / 8) * 4 <= kZeroStride, "zero boxes");
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
-constexpr uint32_t kTmemCols = 2 * BN;  // two 128 x BN fp32 accumulators
+// tensor memory: fp32 accumulator (128 lanes x BT columns), then one A stage
+// (128 lanes x BK / 2 columns: two fp16 per 32-bit cell) per pipeline stage
+constexpr uint32_t kTmemAcc = 0;
+constexpr uint32_t kTmemA = BT;
+constexpr uint32_t kAStageCols = BK / 2;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kTmemA + kStages * kAStageCols <= kTmemCols, "tensor memory budget");
 constexpr long long kWaitLimit = 1ll << 22;  // try_wait rounds before giving up
+
+// K split of grids with few tiles: at most 8 splits, each of at least 8 slabs
+constexpr int kMaxSplit = 8;
+constexpr int kMinSlabsPerSplit = 8;
+constexpr int kSplitSmBound = 256;  // SM count the workspace bound allows for
 
 struct GemmMaps {
   CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 128, 128-byte swizzle
@@ -84,12 +99,12 @@ struct GemmMaps {
 __device__ __forceinline__ int wmap_index(int b) { return b == 8 ? 5 : b - 2; }
 
 struct GemmArgs {
-  const uint32_t* qweight;
-  const uint16_t* scales;
-  const uint32_t* qzeros;
   const uint32_t* seg_off;
   uint16_t* y;
-  int M, N, K, gs, n_word_rows, fmt;
+  float* part;      // [split, M, N] fp32 partial sums when split > 1
+  int M, N, K, gs, n_word_rows;
+  int split;        // CTAs along K (gridDim.z)
+  int slabs_per;    // 64-row slabs per split (the last split may have fewer)
 };
 
 struct StageMeta {  // written by the producer before the stage's copies
@@ -137,14 +152,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
-// Bounded wait by a whole warp: every lane polls, and the loop exits for all
-// lanes in the same round, so warp-collective instructions that follow
-// (tcgen05.ld.sync.aligned, __syncwarp) are always reached convergently.
+// Bounded wait by a whole warp: lane 0 polls and broadcasts, so the loop
+// exits for all lanes in the same round and warp-collective instructions that
+// follow (tcgen05.ld/st.sync.aligned, __syncwarp) are reached convergently.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool leader = (threadIdx.x & 31) == 0;
   for (long long i = 0; i < kWaitLimit; ++i) {
-    const bool done = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    int state = 0;  // 1 = phase complete, 2 = another role gave up
+    if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state == 1) return true;
+    if (state == 2) return false;
   }
   if ((threadIdx.x & 31) == 0) atomicOr(&g_gemm_err, kDevErrTimeout);
   *abort_flag = 1;
@@ -158,8 +176,32 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// the same box into the same shared-memory offset of every CTA in `mask`,
+// completing bytes on the mbarrier at the same offset in each
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// every thread of every CTA in the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -176,22 +218,47 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// instruction descriptor: D fp32, A/B fp16, both K-major, M = 128, N = 256
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(UM >> 4) << 24);
+// instruction descriptor: D fp32, A/B fp16, both K-major, M = 128 (= BN),
+// N = n (a multiple of 16, at most 256)
+__device__ __forceinline__ uint32_t idesc_for(int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(BN >> 4) << 24);
+}
 
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] . B[smem]^T: A (128 x 16 fp16) read from tensor memory
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// one arrival, when this CTA's MMAs so far have completed, on the mbarrier at
+// the same offset in every CTA of `mask`
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(bar), "h"(mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -233,14 +300,18 @@ __device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col
   return natural_order(P);
 }
 
-// the 32 codes of one column of a width-B segment -> 4 swizzled 16-byte
-// chunks (c0 .. c0 + 3) of the column's K-major B-operand row
+// the 32 codes of one column of a width-B segment -> 16 registers of fp16
+// pairs in K order (one TMEM A-operand row of the half slab)
 template <int B>
-__device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint8_t* btile, int c0,
-                                             int sw) {
+__device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint32_t (&r)[16]) {
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
-    *reinterpret_cast<uint4*>(btile + (((c0 + t) ^ sw) << 4)) = exl2_block<B>(rows, t, col, s2);
+  for (int t = 0; t < 4; ++t) {
+    const uint4 o = exl2_block<B>(rows, t, col, s2);
+    r[4 * t + 0] = o.x;
+    r[4 * t + 1] = o.y;
+    r[4 * t + 2] = o.z;
+    r[4 * t + 3] = o.w;
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -252,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* bar_area = smem + kStages * kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
-  uint64_t* bready = full + kStages;
-  uint64_t* empty = bready + kStages;
+  uint64_t* aready = full + kStages;
+  uint64_t* empty = aready + kStages;
   uint64_t* accum = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -261,15 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BM;
-  const int k_tiles = a.K / BK;
-  const int ncols = min(BN, a.N - n0);  // valid columns of this tile (multiple of 128)
+  const int m0 = blockIdx.y * BT;
+  const int kt0 = blockIdx.z * a.slabs_per;                      // this split's first slab
+  const int n_iter = min(a.K / BK, kt0 + a.slabs_per) - kt0;     // >= 1 (host plan)
+  const int tokens = min(BT, a.M - m0);                          // valid tokens of the tile
+  const int n_mma = (tokens + 15) & ~15;                         // MMA N
+  // CTAs of a cluster share the token tile (and K range): each loads 1/cs of
+  // the x rows and multicasts them to all, so a stage is free only when every
+  // CTA's MMAs are done with it
+  const uint32_t crank = cluster_rank(), csize = cluster_size();
+  const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&bready[s]), kDequantWarps);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&aready[s]), kDequantWarps);
+      mbar_init(smem_u32(&empty[s]), csize);
     }
     mbar_init(smem_u32(accum), 1);
     *abort_flag = 0;
@@ -283,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -291,9 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
       int issued = 0;
-      for (int kt = 0; kt < k_tiles; ++kt) {
-        const int s = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
+      for (int i = 0; i < n_iter; ++i) {
+        const int kt = kt0 + i;
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
         if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;
         uint8_t* st = smem + s * kStageBytes;
         const uint32_t bar = smem_u32(&full[s]);
@@ -317,11 +397,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[s].rows0 = rows0;
         meta[s].rows1 = rows1;
         const int rows = rows0 + rows1;
-        // boxes always move their full size (columns past N read as zero)
+        // boxes always move their full size (rows past M and columns past N read as zero)
         uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u + 2u * BN * 2u;
         if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (BN / 8) * 4u;
         mbar_expect_tx(bar, tx);
-        tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
+        if (csize == 1) {
+          tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
+        } else {
+          const int xr = BT / static_cast<int>(csize);  // the tensor map's box height
+          tma_load_2d_mc(smem_u32(st + kOffX + crank * xr * 128), &maps.x, kt * BK, m0 + static_cast<int>(crank) * xr,
+                         bar, cmask);
+        }
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
           tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(8)], n0, row_start, bar);
         } else if (rows > 0) {
@@ -335,117 +421,122 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (FMT == EXQ_FMT_GPTQ4)
             tma_load_2d(smem_u32(st + kOffZero + h * kZeroStride), &maps.z, n0 / 8, g, bar);
         }
-        issued = kt + 1;
+        issued = i + 1;
       }
       // drain: every issued stage's copies must land before the CTA may exit
-      for (int kt = max(0, issued - kStages); kt < issued; ++kt) {
-        const uint32_t bar = smem_u32(&full[kt % kStages]);
-        for (long long i = 0; i < kWaitLimit; ++i)
-          if (mbar_try_wait(bar, (kt / kStages) & 1)) break;
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        const uint32_t bar = smem_u32(&full[i % kStages]);
+        for (long long r = 0; r < kWaitLimit; ++r)
+          if (mbar_try_wait(bar, (i / kStages) & 1)) break;
       }
+      // and every peer's last commits must have arrived on this CTA's barriers
+      if (csize > 1)
+        for (int i = max(0, n_iter - kStages); i < n_iter; ++i) {
+          const uint32_t bar = smem_u32(&empty[i % kStages]);
+          for (long long r = 0; r < kWaitLimit; ++r)
+            if (mbar_try_wait(bar, (i / kStages) & 1)) break;
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int kt = 0; kt < k_tiles; ++kt) {
-        const int s = kt % kStages;
-        const uint32_t ph = (kt / kStages) & 1;
+      const uint32_t idesc = idesc_for(n_mma);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
         if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag)) break;
-        if (!mbar_wait(smem_u32(&bready[s]), ph, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&aready[s]), ph, abort_flag)) break;
         tc_fence_after();
-        uint8_t* st = smem + s * kStageBytes;
-        const uint64_t adesc = sw128_desc(smem_u32(st + kOffX));
-        const uint64_t adesc1 = sw128_desc(smem_u32(st + kOffX + UM * 128));  // rows 128 .. 255
-        const uint64_t bdesc = sw128_desc(smem_u32(st + kOffB));
+        const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes + kOffX));
+        const uint32_t a_tmem = tmem + kTmemA + s * kAStageCols;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {  // +32 bytes along K inside the swizzle atom = +2 encoded
-          umma_f16(tmem, adesc + 2 * k, bdesc + 2 * k, (kt | k) != 0);
-          umma_f16(tmem + BN, adesc1 + 2 * k, bdesc + 2 * k, (kt | k) != 0);
-        }
-        umma_commit(smem_u32(&empty[s]));
+        for (int k = 0; k < BK / 16; ++k)  // K = 16: 8 TMEM columns of A; +32 bytes of x = +2 encoded
+          umma_f16_ts(tmem + kTmemAcc, a_tmem + 8 * k, bdesc + 2 * k, idesc, (i | k) != 0);
+        if (csize == 1) umma_commit(smem_u32(&empty[s]));
+        else umma_commit_mc(smem_u32(&empty[s]), cmask);
       }
       umma_commit(smem_u32(accum));
     }
   } else {
     // ------------------------------------------------------------ dequantisers
-    const int dw = warp - 2;
-    const int col = (dw & 3) * 32 + lane;  // output column of this thread inside the tile
-    const int h = dw >> 2;                 // its 32-row half of the 64-row K slab
-    for (int kt = 0; kt < k_tiles; ++kt) {
-      const int s = kt % kStages;
-      const uint32_t ph = (kt / kStages) & 1;
+    const int q = warp & 3;                      // the TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;               // its 32-row half of the slab
+    const int col = q * 32 + lane;               // output column in the tile = A row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    for (int i = 0; i < n_iter; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
       if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort_flag)) break;
-      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;  // B buffer consumed
-      uint8_t* st = smem + s * kStageBytes;
+      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;  // A stage read by earlier MMAs
+      tc_fence_after();
+      const uint8_t* st = smem + s * kStageBytes;
       const uint32_t* packed = reinterpret_cast<const uint32_t*>(st + kOffPacked);
       const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
-      uint8_t* btile = st + kOffB + (col >> 3) * 1024 + (col & 7) * 128;
-      const int sw = col & 7;
-      {
-        const uint32_t s16 = sc[h * BN + col];
-        const uint32_t s2 = s16 | (s16 << 16);
-        if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
-          uint32_t zlo, zhi;
-          gptq_zero_consts((zw >> (4 * (col & 7))) & 0xFu, zlo, zhi);
+      const uint32_t s16 = sc[h * BN + col];
+      const uint32_t s2 = s16 | (s16 << 16);
+      uint32_t r[16];
+      if constexpr (FMT == EXQ_FMT_GPTQ4) {
+        const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
+        uint32_t zlo, zhi;
+        gptq_zero_consts((zw >> (4 * (col & 7))) & 0xFu, zlo, zhi);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint32_t P[4];
-            unpack8_gptq(packed[(4 * h + t) * BN + col], zlo, zhi, P);
+        for (int t = 0; t < 4; ++t) {
+          uint32_t P[4];
+          unpack8_gptq(packed[(4 * h + t) * BN + col], zlo, zhi, P);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) P[i] = hmul2(P[i], s2);
-            const int c = 4 * h + t;  // 16-byte chunk along K
-            *reinterpret_cast<uint4*>(btile + ((c ^ sw) << 4)) = natural_order(P);
-          }
-        } else {
-          const int b = h == 0 ? meta[s].rows0 : meta[s].rows1;
-          const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
-          // one branch per 32-row segment, each width's 4 blocks unrolled inside
-          switch (b) {
-            case 2: exl2_segment<2>(rows, col, s2, btile, 4 * h, sw); break;
-            case 3: exl2_segment<3>(rows, col, s2, btile, 4 * h, sw); break;
-            case 4: exl2_segment<4>(rows, col, s2, btile, 4 * h, sw); break;
-            case 5: exl2_segment<5>(rows, col, s2, btile, 4 * h, sw); break;
-            case 6: exl2_segment<6>(rows, col, s2, btile, 4 * h, sw); break;
-            case 8: exl2_segment<8>(rows, col, s2, btile, 4 * h, sw); break;
-            default:
+          for (int j = 0; j < 4; ++j) P[j] = hmul2(P[j], s2);
+          const uint4 o = natural_order(P);
+          r[4 * t + 0] = o.x;
+          r[4 * t + 1] = o.y;
+          r[4 * t + 2] = o.z;
+          r[4 * t + 3] = o.w;
+        }
+      } else {
+        const int b = h == 0 ? meta[s].rows0 : meta[s].rows1;
+        const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
+        // one branch per 32-row segment (warp-uniform), each width's 4 blocks unrolled inside
+        switch (b) {
+          case 2: exl2_segment<2>(rows, col, s2, r); break;
+          case 3: exl2_segment<3>(rows, col, s2, r); break;
+          case 4: exl2_segment<4>(rows, col, s2, r); break;
+          case 5: exl2_segment<5>(rows, col, s2, r); break;
+          case 6: exl2_segment<6>(rows, col, s2, r); break;
+          case 8: exl2_segment<8>(rows, col, s2, r); break;
+          default:
 #pragma unroll
-              for (int t = 0; t < 4; ++t)
-                *reinterpret_cast<uint4*>(btile + (((4 * h + t) ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
-          }
+            for (int j = 0; j < 16; ++j) r[j] = 0u;
         }
       }
-      fence_proxy_async_smem();  // make the generic-proxy writes visible to the tensor cores
+      tmem_st16(tmem + lane_base + kTmemA + s * kAStageCols + h * 16, r);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bready[s]));
+      if (lane == 0) mbar_arrive(smem_u32(&aready[s]));
     }
 
     // ------------------------------------------------------------ epilogue
+    // accumulator lane = output column, accumulator column = token; warp h
+    // takes tokens [128 h, 128 h + 128) of its lane quarter
     if (mbar_wait_warp(smem_u32(accum), 0, abort_flag)) {
       tc_fence_after();
-      const int quarter = warp & 3;          // TMEM lanes this warp may read
-      const int acc = dw >> 2;               // which accumulator (rows 0..127 or 128..255)
-      const int m = m0 + acc * UM + quarter * 32 + lane;
+      const int n = n0 + col;
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        const int c0 = cc * 32;
+      for (int cc = 0; cc < 4; ++cc) {
+        const int t0 = h * 128 + cc * 32;
+        if (t0 >= tokens) break;  // warp-uniform
         uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + c0, r);
-        if (m < a.M && c0 < ncols) {
-          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(m) * a.N + n0 + c0);
+        tmem_ld32(tmem + lane_base + kTmemAcc + t0, r);
+        const int mt = tokens - t0;
+        if (a.split == 1) {
+          uint16_t* dst = a.y + static_cast<size_t>(m0 + t0) * a.N + n;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 0]))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 1])))) << 16);
-            o.y = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 2]))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 3])))) << 16);
-            o.z = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 4]))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 5])))) << 16);
-            o.w = __half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 6]))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(__uint_as_float(r[8 * q + 7])))) << 16);
-            dst[q] = o;
-          }
+          for (int j = 0; j < 32; ++j)
+            if (j < mt) dst[static_cast<size_t>(j) * a.N] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
+        } else {
+          float* dst = a.part + (static_cast<size_t>(blockIdx.z) * a.M + m0 + t0) * a.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < mt) dst[static_cast<size_t>(j) * a.N] = __uint_as_float(r[j]);
         }
       }
     }
@@ -453,9 +544,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (csize > 1) cluster_sync();  // no CTA leaves while a peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// y = fp16(sum over splits of the fp32 partial sums), added in split order so
+// the result does not depend on which CTA finished first. Launched as a
+// programmatic dependent of the split GEMM.
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y,
+                                                           long long mn, int split) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x * 8;
+  for (long long e = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; e < mn; e += stride) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int z = 0; z < split; ++z) {
+      const float4* p = reinterpret_cast<const float4*>(part + z * mn + e);
+      const float4 u = __ldg(p), v = __ldg(p + 1);
+      acc[0] += u.x; acc[1] += u.y; acc[2] += u.z; acc[3] += u.w;
+      acc[4] += v.x; acc[5] += v.y; acc[6] += v.z; acc[7] += v.w;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = __half_as_ushort(__float2half_rn(acc[2 * j])) |
+             (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc[2 * j + 1]))) << 16);
+    *reinterpret_cast<uint4*>(y + e) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -500,15 +618,65 @@ EncodeTiled encode_fn() {
 
 }  // namespace
 
-size_t gemm_workspace_bytes(const exq_weight& w, int M) {
-  return w.perm ? static_cast<size_t>(M) * w.K * 2 : 0;
+namespace {
+
+struct SplitPlan {
+  int split;      // CTAs along K
+  int slabs_per;  // 64-row slabs per split
+};
+
+// A grid of fewer than half an SM count of tiles is split along K: as many
+// splits as fill the SMs, at most kMaxSplit, each of at least
+// kMinSlabsPerSplit slabs, rounded so that no split is empty.
+SplitPlan plan_split(int tiles, int slabs, int sms) {
+  int s = 1;
+  if (tiles * 2 <= sms) s = std::min(std::min(kMaxSplit, sms / tiles), slabs / kMinSlabsPerSplit);
+  if (s < 1) s = 1;
+  const int per = (slabs + s - 1) / s;
+  return {(slabs + per - 1) / per, per};
 }
 
-exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace, size_t,
+size_t gather_bytes(const exq_weight& w, int M) {
+  return w.perm ? ((static_cast<size_t>(M) * w.K * 2 + 255) / 256) * 256 : 0;
+}
+
+size_t partial_bytes(const exq_weight& w, int M, int split) {
+  return split > 1 ? static_cast<size_t>(split) * M * w.N * 4 : 0;
+}
+
+int tiles_of(const exq_weight& w, int M) { return (w.N / BN) * ((M + BT - 1) / BT); }
+
+// CTAs per cluster along the column tiles (they share each x tile by multicast)
+int cluster_for(int n_tiles) { return n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1); }
+
+}  // namespace
+
+// Gathered activations (act-order) plus the fp32 partial sums of the largest
+// K split any device up to kSplitSmBound SMs would choose; the launch uses the
+// split of the actual device, which never needs more.
+size_t gemm_workspace_bytes(const exq_weight& w, int M) {
+  size_t bytes = gather_bytes(w, M);
+  if (w.K % BK == 0 && w.N % BN == 0 && M >= 1)
+    bytes += partial_bytes(w, M, plan_split(tiles_of(w, M), w.K / BK, kSplitSmBound).split);
+  return bytes;
+}
+
+size_t gemm_gather_bytes(const exq_weight& w, int M) { return gather_bytes(w, M); }
+
+exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace, size_t ws_bytes,
                        cudaStream_t stream) {
-  if (w.K % BK || w.N % 128) return EXQ_ERR_UNSUPPORTED;
+  if (w.K % BK || w.N % BN) return EXQ_ERR_UNSUPPORTED;
   EncodeTiled enc = encode_fn();
   if (!enc) return EXQ_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
+  const int sms = std::min(device_info(dev).sm_count, kSplitSmBound);
+
+  const int slabs = w.K / BK;
+  SplitPlan plan = plan_split(tiles_of(w, M), slabs, sms);
+  const size_t gbytes = gather_bytes(w, M);
+  if (plan.split > 1 && (!workspace || gbytes + partial_bytes(w, M, plan.split) > ws_bytes)) plan = {1, slabs};
+  float* part = plan.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gbytes) : nullptr;
 
   const uint16_t* xa = x;
   if (w.perm) {
@@ -520,13 +688,14 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     xa = xp;
   }
 
+  const int cs = cluster_for(w.N / BN);
   GemmMaps maps;
   std::memset(&maps, 0, sizeof maps);
   const cuuint32_t es[2] = {1, 1};
   {
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
-    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BT / cs)};
     if (enc(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -563,25 +732,54 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   }
 
   GemmArgs args{};
-  args.qweight = w.qweight;
-  args.scales = w.scales;
-  args.qzeros = w.qzeros;
   args.seg_off = w.seg_word_off;
   args.y = y;
+  args.part = part;
   args.M = M;
   args.N = w.N;
   args.K = w.K;
   args.gs = w.group_size;
   args.n_word_rows = w.n_word_rows;
-  args.fmt = w.format;
+  args.split = plan.split;
+  args.slabs_per = plan.slabs_per;
 
   auto fn = w.format == EXQ_FMT_GPTQ4 ? gemm_kernel<EXQ_FMT_GPTQ4> : gemm_kernel<EXQ_FMT_EXL2>;
   static std::once_flag attr_once[2];
   std::call_once(attr_once[w.format == EXQ_FMT_GPTQ4 ? 0 : 1],
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
-  const dim3 grid((w.N + BN - 1) / BN, (M + BM - 1) / BM, 1);
-  fn<<<grid, kThreads, kSmemBytes, stream>>>(maps, args);
-  if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
+  {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(w.N / BN, (M + BT - 1) / BT, plan.split);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fn, maps, args) != cudaSuccess) return EXQ_ERR_CUDA;
+  }
+
+  if (plan.split > 1) {
+    const long long mn = static_cast<long long>(M) * w.N;
+    const long long vecs = mn / 8;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<long long>((vecs + 255) / 256, 8LL * sms)));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(part), y, mn, plan.split) !=
+        cudaSuccess)
+      return EXQ_ERR_CUDA;
+  }
   return EXQ_OK;
 }
 
@@ -611,7 +809,7 @@ void* noalloc_scratch(int dev) {
 }  // namespace
 
 exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream) {
-  const size_t need = gemm_workspace_bytes(w, M);
+  const size_t need = gather_bytes(w, M);
   if (need > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (need) {

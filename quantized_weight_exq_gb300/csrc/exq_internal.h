@@ -31,6 +31,8 @@ exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t str
 exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_bytes(const exq_weight& w, int M);
+// the act-order part of it: M * K * 2 rounded up to 256 bytes, 0 without a permutation
+size_t gemm_gather_bytes(const exq_weight& w, int M);
 // exq_gemm with the library's static scratch array as the workspace
 exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream);
 

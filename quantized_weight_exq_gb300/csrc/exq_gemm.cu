@@ -176,34 +176,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// the same box into the same shared-memory offset of every CTA in `mask`,
-// completing bytes on the mbarrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-// every thread of every CTA in the cluster
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -250,15 +222,6 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-
-// one arrival, when this CTA's MMAs so far have completed, on the mbarrier at
-// the same offset in every CTA of `mask`
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(bar), "h"(mask)
-      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -337,17 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_iter = min(a.K / BK, kt0 + a.slabs_per) - kt0;     // >= 1 (host plan)
   const int tokens = min(BT, a.M - m0);                          // valid tokens of the tile
   const int n_mma = (tokens + 15) & ~15;                         // MMA N
-  // CTAs of a cluster share the token tile (and K range): each loads 1/cs of
-  // the x rows and multicasts them to all, so a stage is free only when every
-  // CTA's MMAs are done with it
-  const uint32_t crank = cluster_rank(), csize = cluster_size();
-  const uint16_t cmask = static_cast<uint16_t>((1u << csize) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&aready[s]), kDequantWarps);
-      mbar_init(smem_u32(&empty[s]), csize);
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(accum), 1);
     *abort_flag = 0;
@@ -361,7 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (csize > 1) cluster_sync();  // peers' barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -401,13 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u + 2u * BN * 2u;
         if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (BN / 8) * 4u;
         mbar_expect_tx(bar, tx);
-        if (csize == 1) {
-          tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
-        } else {
-          const int xr = BT / static_cast<int>(csize);  // the tensor map's box height
-          tma_load_2d_mc(smem_u32(st + kOffX + crank * xr * 128), &maps.x, kt * BK, m0 + static_cast<int>(crank) * xr,
-                         bar, cmask);
-        }
+        tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
           tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(8)], n0, row_start, bar);
         } else if (rows > 0) {
@@ -429,13 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long r = 0; r < kWaitLimit; ++r)
           if (mbar_try_wait(bar, (i / kStages) & 1)) break;
       }
-      // and every peer's last commits must have arrived on this CTA's barriers
-      if (csize > 1)
-        for (int i = max(0, n_iter - kStages); i < n_iter; ++i) {
-          const uint32_t bar = smem_u32(&empty[i % kStages]);
-          for (long long r = 0; r < kWaitLimit; ++r)
-            if (mbar_try_wait(bar, (i / kStages) & 1)) break;
-        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -452,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)  // K = 16: 8 TMEM columns of A; +32 bytes of x = +2 encoded
           umma_f16_ts(tmem + kTmemAcc, a_tmem + 8 * k, bdesc + 2 * k, idesc, (i | k) != 0);
-        if (csize == 1) umma_commit(smem_u32(&empty[s]));
-        else umma_commit_mc(smem_u32(&empty[s]), cmask);
+        umma_commit(smem_u32(&empty[s]));
       }
       umma_commit(smem_u32(accum));
     }
@@ -544,7 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (csize > 1) cluster_sync();  // no CTA leaves while a peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -598,24 +540,6 @@ __global__ void permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* 
   }
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  });
-  return fn;
-}
-
 }  // namespace
 
 namespace {
@@ -646,9 +570,6 @@ size_t partial_bytes(const exq_weight& w, int M, int split) {
 
 int tiles_of(const exq_weight& w, int M) { return (w.N / BN) * ((M + BT - 1) / BT); }
 
-// CTAs per cluster along the column tiles (they share each x tile by multicast)
-int cluster_for(int n_tiles) { return n_tiles % 4 == 0 ? 4 : (n_tiles % 2 == 0 ? 2 : 1); }
-
 }  // namespace
 
 // Gathered activations (act-order) plus the fp32 partial sums of the largest
@@ -666,7 +587,7 @@ size_t gemm_gather_bytes(const exq_weight& w, int M) { return gather_bytes(w, M)
 exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace, size_t ws_bytes,
                        cudaStream_t stream) {
   if (w.K % BK || w.N % BN) return EXQ_ERR_UNSUPPORTED;
-  EncodeTiled enc = encode_fn();
+  EncodeTiled enc = tensor_map_encoder();
   if (!enc) return EXQ_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
@@ -688,14 +609,13 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     xa = xp;
   }
 
-  const int cs = cluster_for(w.N / BN);
   GemmMaps maps;
   std::memset(&maps, 0, sizeof maps);
   const cuuint32_t es[2] = {1, 1};
   {
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
-    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BT / cs)};
+    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BT)};
     if (enc(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -753,13 +673,6 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, fn, maps, args) != cudaSuccess) return EXQ_ERR_CUDA;
   }
 

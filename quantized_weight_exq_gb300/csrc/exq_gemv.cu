@@ -9,43 +9,48 @@
 // weights stream in stored order.
 //
 // GB300 mapping:
-//  * Work is the set of (256-column tile, 32-row step) pairs, ordered by K
-//    chunk (a chunk is as many steps as the staged activations fit in shared
-//    memory), then tile, then step. Every CTA (one per SM) takes an equal
-//    contiguous share, so all SMs stream the same number of bytes whatever N
-//    and K are. A share falls into pieces, one per tile it touches.
-//  * Inside a piece the warps form 4 column groups (64 columns each) x KG K
-//    groups; a K group owns a contiguous run of the piece's steps, and the 4
-//    warps of a K group read the same word rows side by side (1 KB per row).
-//  * Per step a lane (g = lane / 4, t = lane % 4) owns 8 columns (4g .. 4g+3
-//    and 32+4g .. 32+4g+3 of its group) of the 8-row block t of the step: the
-//    8 lanes of a word row read whole 128-byte lines. Its word rows and scales
-//    travel by cp.async into a private slot of a P-stage shared-memory ring,
-//    so P - 1 steps of every lane are in flight while it works on the current
-//    one, with no cross-warp hand-shake; the fetches run ahead across piece
-//    boundaries.
-//  * Codes are planted in the mantissa of 1024 (0x6400 | code << p), the zero
-//    is taken off exactly in fp16 and each pair is scaled once
-//    (w = fp16_RN((q - z) s), the definition), then fed to mma.sync m16n8k16
-//    (fp16 in, fp32 accumulate) as the A operand of a swapped product
-//    (A = W^T, B = x^T). The K order inside a 16-slab is free as long as A and
-//    B agree, so x is staged in the pair order the unpackers produce.
-//  * At the end of a piece the K groups' partial sums are added in shared
-//    memory in K-group order. A tile that one CTA covers whole is written to
-//    y; the pieces of a shared tile go to the caller's workspace and the CTA
-//    that arrives last (one atomic counter per tile) adds them in piece order,
-//    writes y and puts the counter back to zero. Deterministic, and no CTA
-//    ever waits on another.
+//  * Work is the list of (248-column tile, 32-row segment) units, tile-major.
+//    Every CTA (one per SM) takes an equal contiguous share, so all SMs
+//    stream the same number of bytes whatever N and K are. A share falls into
+//    pieces, one per tile it touches.
+//  * Warp 16 is the producer. It cuts each piece into stages of at most eight
+//    segments (256 rows of K) and at most 32 packed word rows, and moves a
+//    stage with three tensor-map copies into one slot of a shared-memory ring:
+//    the word rows (a 32-row x 248-column box), the scale rows (an 8 x 248
+//    box) and the stage's activations (a 256 x M box); GPTQ zero rows follow
+//    as 4-byte asynchronous copies. All of it completes on the slot's "full"
+//    mbarrier. The weight copies of the first slots are issued before the
+//    wait on the previous kernel (they are model state); x after it.
+//  * Warps 0-15 consume: warp w owns columns 32 (w % 8) .. +31 of the tile and
+//    the stage's even (w < 8) or odd (w >= 8) segments, so no partial sums
+//    cross warps inside the CTA. Lane (g = lane / 4, t = lane % 4) owns the
+//    four columns 4g .. 4g+3 (one 16-byte read per word row: eight lanes read
+//    a whole line) and the 8-code block t of every segment. The tile is 248
+//    columns wide so that a word row takes 992 bytes in shared memory: the
+//    four rows that the lanes t = 0..3 of one quarter-warp read then start 6
+//    bank groups apart, and their 16-byte reads do not collide (2-, 3-, 4- and
+//    5-bit segments; 6- and 8-bit ones keep a two-way overlap). Codes are
+//    planted in the mantissa of 1024 (0x6400 | code << p), the zero is taken
+//    off exactly in fp16 and each pair is scaled once (w = fp16_RN((q - z) s),
+//    the definition: the result is x times the rounded fp16 weights), then
+//    fed to mma.sync m16n8k16 (fp16 in, fp32 accumulate) as the A operand of a
+//    swapped product (A = W^T, B = x^T).
+//  * At the end of a piece each warp writes fp32 partial sums of its 32
+//    columns and K group to the caller's workspace; the warp that arrives
+//    last at its (tile, column group) counter adds the tile's partials in
+//    piece order, writes y and puts the counter back to zero. Deterministic,
+//    and no warp ever waits on another CTA.
 //  * An act-order layer's x is gathered into stored-row order by a small
-//    kernel first (into the workspace), once per call rather than once per
-//    CTA.
-//  * Programmatic dependent launch: the kernels let the next launch start
-//    early; the GEMV starts fetching weights before it waits for the previous
-//    kernel; x, y and the workspace are touched only after that wait.
+//    kernel first (into the workspace), once per call rather than per CTA.
+//  * Programmatic dependent launch: every kernel lets the next launch start
+//    early; the GEMV's first weight copies do not wait for the previous
+//    kernel, its activations and outputs do.
+//  * Every mbarrier wait is bounded; on expiry the kernel records a timeout
+//    in its device error word and the other roles stop at their next wait.
 #include <algorithm>
-#include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "exq_device.cuh"
@@ -56,39 +61,70 @@ namespace {
 
 __device__ unsigned g_gemv_err;
 
-constexpr int kTN = 256;                     // columns per tile
-constexpr int kCG = 4;                       // 64-column groups of a tile, one per warp of a K group
-constexpr int kCounterBytes = 64 * 1024;     // workspace counter region (zero between calls)
-constexpr int kP = 4;                        // pipeline stages per lane
-constexpr int kSlotBytes = 80;               // per lane and stage: a0 a1 | b0 b1 | scales
+constexpr int kTN = 248;                 // columns per tile (992-byte rows: see above)
+constexpr int kTP = 256;                 // columns per tile in the partial sums (8 warps x 32)
+constexpr int kColGroups = 8;            // 32 columns each
+constexpr int kConsumerWarps = 2 * kColGroups;  // two K groups: even / odd segments of a stage
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kSegsPerStage = 8;         // 256 rows of K
+constexpr int kRowsPerStage = 32;        // packed word rows per stage (box height)
+constexpr int kScaleRows = 8;            // scale (and GPTQ zero) rows per stage
+constexpr int kCounterBytes = 64 * 1024; // workspace counter region (zero between calls)
+constexpr int kMaxStages = 6;
+constexpr long long kWaitLimit = 1ll << 17;  // try_wait rounds (each may sleep kWaitHintNs) before giving up
+constexpr uint32_t kWaitHintNs = 20000;      // a waiting thread sleeps until the phase completes or this long
 
-// Launch shapes: M <= 8 with 16 warps (4 column groups x 4 K groups); M <= 16
-// (two 8-token blocks) with 8 (4 x 2).
-__host__ __device__ constexpr int mode_for(int M) { return M <= 8 ? 0 : 1; }
-__host__ __device__ constexpr int warps_of(int mode) { return mode == 0 ? 16 : 8; }
+// slot layout (bytes): word rows | scale rows | GPTQ zero rows | x [M][128]
+constexpr int kRowBytes = kTN * 4;                       // 992
+constexpr int kSlotW = 0;
+constexpr int kSlotS = kSlotW + kRowsPerStage * kRowBytes;
+constexpr int kSlotZ = ((kSlotS + kScaleRows * kTN * 2 + 127) / 128) * 128;
+constexpr int kZeroRowBytes = 128;                         // 31 zero words of a tile, one row per group
+constexpr int kSlotX = kSlotZ + kScaleRows * kZeroRowBytes;
+constexpr int kXRowBytes = kSegsPerStage * 32 * 2;         // 512 B per token
+static_assert(kSlotS % 128 == 0 && kSlotX % 128 == 0, "tensor-map destinations start on 128-byte boundaries");
+static_assert(kTN % 8 == 0 && kTN / 8 <= 32, "a tile's zero words fit one warp");
+
+__host__ __device__ constexpr int slot_bytes_for(int M) { return ((kSlotX + M * kXRowBytes + 1023) / 1024) * 1024; }
+
+struct GemvMaps {
+  CUtensorMap w;  // qweight [n_word_rows, N] uint32, box 248 x 16
+  CUtensorMap s;  // scales [groups, N] fp16, box 248 x 4
+  CUtensorMap x;  // activations [M, K] fp16 (stored-row order), box 128 x M
+};
 
 struct GemvArgs {
-  const uint32_t* qweight;
-  const uint16_t* scales;
-  const uint32_t* qzeros;
-  const uint32_t* seg_off;
-  const uint16_t* x;
+  const uint32_t* seg_off;  // EXL2 [S + 1]
+  const uint32_t* qzeros;   // GPTQ [G, N / 8]
   uint16_t* y;
-  uint32_t* counters;   // [n_tiles], zero between calls
-  float* partials;      // [n_tiles][max_pieces][M][kTN]
+  uint32_t* counters;       // [n_tiles][8], zero between calls
+  float* partials;          // [n_tiles][max_pieces][M][kTP]
   int K, N, M;
-  int n_steps;          // K / 32
-  int gs_steps;         // GPTQ: group_size / 32; EXL2: 1
+  int S;                    // segments (K / 32)
+  int gs_seg;               // GPTQ group size in segments
+  int G;                    // GPTQ groups
   int n_word_rows;
-  int n_tiles;          // ceil(N / kTN)
-  int kc_steps;         // steps per K chunk
-  int n_chunks;
+  int n_tiles;
+  int total;                // units = n_tiles * S
   int max_pieces;
-  int xs_stride;        // halves per staged x row
-  int total;            // n_tiles * n_steps
-  // byte offsets in dynamic shared memory (from a 1024-aligned base)
-  int off_flags, off_x, off_meta, off_red;
+  int stages;
+  int slot_bytes;
+  int off_bar;              // byte offset of the barriers, descriptors and table
 };
+
+// Stage descriptor, written by the producer before the slot's copies.
+// The consumer K groups take the first h = (count + 1) / 2 segments and the rest.
+//   a: first segment | count << 16 | first-of-piece << 20 | last-of-piece << 21
+//      | end << 22 | H << 24, H = the second half's first word row in the slot
+//      (EXL2) or its scale / zero row (GPTQ)
+//   b: EXL2: widths, 4 bits per segment (0 = skip the segment);
+//      GPTQ: position in its group of the first segment | of the second half's << 16
+//   c: tile
+//   d: first scale row of the slot (GPTQ group / EXL2 segment)
+struct Desc {
+  uint32_t a, b, c, d;
+};
+constexpr uint32_t kDescFirst = 1u << 20, kDescLast = 1u << 21, kDescEnd = 1u << 22;
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -96,10 +132,64 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// barrier of all NW warps of the CTA (id 1; __syncthreads uses 0)
-template <int NW>
-__device__ __forceinline__ void cta_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by lane 0 of a warp, result broadcast to the warp (all lanes
+// leave in the same round). A timeout is recorded and raises the abort flag;
+// a raised flag makes every other waiter give up too.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool leader = (threadIdx.x & 31) == 0;
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    int state = 0;  // 1 = phase complete, 2 = another role gave up
+    if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state == 1) return true;
+    if (state == 2) return false;
+  }
+  if (leader) {
+    atomicOr(&g_gemv_err, kDevErrTimeout);
+    *abort_flag = 1;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// 4-byte asynchronous copy; cp_async_arrive adds one pending arrival to
+// `bar` at once and makes it when all of this thread's earlier cp.async
+// copies have landed
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -111,197 +201,118 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// shared-memory reads through plain pointers: ordered after the mbarrier
+// waits (asm volatile with a memory clobber) and free to be scheduled
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
 __device__ __forceinline__ uint32_t comp(const uint4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
-// 16-, 8- and 4-byte asynchronous global -> shared copies, one per thread,
-// tracked per thread in commit groups
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
-// ---------------------------------------------------------------- work split
-// The work is the list of (chunk, tile, step) positions in that order
-// (total < 2^31, checked on the host); CTA c owns [c * total / G,
-// (c + 1) * total / G).
-
-struct Split {
-  int total, G, n_tiles, n_steps, kc_steps, n_chunks;
-
-  __host__ __device__ int begin(int c) const {
-    return static_cast<int>(static_cast<long long>(c) * total / G);
-  }
-  // the CTA that owns position p
-  __host__ __device__ int owner(int p) const {
-    return static_cast<int>((static_cast<long long>(p + 1) * G - 1) / total);
-  }
-  __host__ __device__ int chunk_len(int kc) const {
-    return kc == n_chunks - 1 ? n_steps - kc * kc_steps : kc_steps;
-  }
-  __host__ __device__ int unit_begin(int kc, int tile) const {
-    return kc * n_tiles * kc_steps + tile * chunk_len(kc);
-  }
-  // CTAs sharing unit (kc, tile) and the first of them
-  __host__ __device__ int unit_pieces(int kc, int tile, int& first) const {
-    const int u0 = unit_begin(kc, tile);
-    first = owner(u0);
-    return owner(u0 + chunk_len(kc) - 1) - first + 1;
-  }
-};
-
-struct Piece {
-  int kc, tile;
-  int sa, sb;     // absolute steps [sa, sb)
-  int slot, P;    // index among the tile's pieces, number of pieces
-};
-
-// the piece that starts at position p (< end) of CTA c's share
-__device__ __forceinline__ Piece piece_at(const Split& sp, int c, int p, int end, int& next) {
-  Piece pc;
-  const int per_chunk = sp.n_tiles * sp.kc_steps;
-  pc.kc = min(p / per_chunk, sp.n_chunks - 1);
-  const int base = pc.kc * per_chunk;
-  const int len = sp.chunk_len(pc.kc);
-  const int rem = p - base;
-  pc.tile = rem / len;
-  const int sin = rem - pc.tile * len;
-  next = min(end, base + (pc.tile + 1) * len);
-  pc.sa = pc.kc * sp.kc_steps + sin;
-  pc.sb = pc.sa + (next - p);
-  pc.P = 0;
-  pc.slot = 0;
-  for (int k = 0; k < sp.n_chunks; ++k) {
-    int first;
-    const int n = sp.unit_pieces(k, pc.tile, first);
-    if (k < pc.kc) pc.slot += n;
-    if (k == pc.kc) pc.slot += c - first;
-    pc.P += n;
-  }
-  return pc;
-}
-
-// steps [ws, we) of warp w (of NW) inside a piece
-template <int NW>
-__device__ __forceinline__ void warp_range(const Piece& pc, int w, int& ws, int& we) {
-  const int len = pc.sb - pc.sa;
-  const int L = (len + NW - 1) / NW;
-  ws = min(pc.sb, pc.sa + w * L);
-  we = min(pc.sb, ws + L);
-}
-
-// ---------------------------------------------------------------- one 32-row step
-// Lane column c (0..7) is column 4g + c (c < 4) or 32 + 4g + c - 4 of the
-// warp's 64-column group.
-
-__device__ __forceinline__ int group_col(int c, int g) { return (c < 4 ? 0 : 28) + 4 * g + c; }
+// ---------------------------------------------------------------- one segment
+// Lane (g, t) holds, for its four columns c = 0..3, the exact fp16 pairs
+// P[c][i] = (v_i - z, v_{i+4} - z) of the codes v_0..v_7 of block t. The MMA
+// rows are the columns: tile 0 = columns 0 (row g) and 1 (row g + 8), tile 1
+// = columns 2 and 3. Slab 0 takes pairs 0 and 1, slab 1 pairs 2 and 3; the
+// activations xb[mt] hold the matching pairs of token g (+ 8 mt).
 
 template <int MT>
-__device__ __forceinline__ void zero_acc(float (&a)[MT][4][4]) {
+__device__ __forceinline__ void seg_mma(float (&D)[MT][2][4], const uint32_t (&P)[4][4], const uint32_t (&xb)[MT][4]) {
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * h;
+      mma16816(D[mt][h], P[c][0], P[c + 1][0], P[c][1], P[c + 1][1], xb[mt][0], xb[mt][1]);
+      mma16816(D[mt][h], P[c][2], P[c + 1][2], P[c][3], P[c + 1][3], xb[mt][2], xb[mt][3]);
+    }
+  }
+}
+
+// EXL2 width B: `row` points at the lane's first word row of block t (the
+// lane's four columns), `off` is the block's bit offset in it.
+template <int B>
+__device__ __forceinline__ void exl2_unpack(const uint8_t* row, uint32_t off, uint32_t (&P)[4][4]) {
+  const uint4 wa = lds128(row);
+  uint4 wb = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (B == 3 || B == 5 || B == 6 || B == 8) wb = lds128(row + kRowBytes);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t a = comp(wa, c);
+    uint32_t lo = a, hi = 0u;
+    if constexpr (B == 2) {
+      lo = a >> off;
+    } else if constexpr (B == 8) {
+      hi = comp(wb, c);
+    } else if constexpr (B == 3 || B == 5 || B == 6) {
+      const uint32_t b = comp(wb, c);
+      lo = fshr(a, b, off);
+      hi = b >> off;
+    }
+    unpack8<B>(lo, hi, P[c]);
+  }
+}
+
+// the lane's four scales of one scale row, each in both halves of a word
+__device__ __forceinline__ void scales4(const uint8_t* p, uint32_t (&s2)[4]) {
+  const uint2 v = lds64(p);
+  s2[0] = prmt(v.x, v.x, 0x1010);
+  s2[1] = prmt(v.x, v.x, 0x3232);
+  s2[2] = prmt(v.y, v.y, 0x1010);
+  s2[3] = prmt(v.y, v.y, 0x3232);
+}
+
+// w = fp16_RN((q - z) s) for the lane's four columns
+__device__ __forceinline__ void scale_pairs(uint32_t (&P)[4][4], const uint32_t (&s2)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) P[c][i] = hmul2(P[c][i], s2[c]);
+}
+
+// one EXL2 segment of width B, whole: unpack, scale, multiply (each width
+// keeps its own registers from the unpack to the MMA)
+template <int B, int MT>
+__device__ __forceinline__ void exl2_seg(const uint8_t* row, uint32_t off, const uint32_t (&xb)[MT][4],
+                                         const uint32_t (&s2)[4], float (&acc)[MT][2][4]) {
+  uint32_t P[4][4];
+  exl2_unpack<B>(row, off, P);
+  scale_pairs(P, s2);
+  seg_mma<MT>(acc, P, xb);
+}
+
+template <int MT>
+__device__ __forceinline__ void zero4(float (&a)[MT][2][4]) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[mt][nt][i] = 0.f;
+      for (int i = 0; i < 4; ++i) a[mt][h][i] = 0.f;
 }
 
-template <int MT>
-__device__ __forceinline__ void mma_pair(float (&acc)[MT][4][4], int nt, const uint32_t (&P0)[4],
-                                         const uint32_t (&P1)[4], const uint4& xb0, const uint4& xb1) {
-  // A rows g / g + 8 = half columns 2nt / 2nt + 1; slab 0 takes pairs
-  // 0 (k 2t, 2t+1) and 1 (k 2t+8, 2t+9), slab 1 pairs 2 and 3
-  mma16816(acc[0][nt], P0[0], P1[0], P0[1], P1[1], xb0.x, xb0.y);
-  mma16816(acc[0][nt], P0[2], P1[2], P0[3], P1[3], xb0.z, xb0.w);
-  if constexpr (MT == 2) {
-    mma16816(acc[1][nt], P0[0], P1[0], P0[1], P1[1], xb1.x, xb1.y);
-    mma16816(acc[1][nt], P0[2], P1[2], P0[3], P1[3], xb1.z, xb1.w);
-  }
+// the pairs (x0,x4),(x1,x5),(x2,x6),(x3,x7) of 8 consecutive activations
+__device__ __forceinline__ void x_pairs(const uint8_t* p, uint32_t (&xb)[4]) {
+  const uint4 v = lds128(p);
+  xb[0] = prmt(v.x, v.z, 0x5410);
+  xb[1] = prmt(v.x, v.z, 0x7632);
+  xb[2] = prmt(v.y, v.w, 0x5410);
+  xb[3] = prmt(v.y, v.w, 0x7632);
 }
 
-// (s, s) of half column c from the half's 8 scales in v
-__device__ __forceinline__ uint32_t scale_x2(const uint4& v, int c) {
-  const uint32_t h = comp(v, c >> 1);
-  return (c & 1) ? prmt(h, h, 0x3232) : prmt(h, h, 0x1010);
+// ---------------------------------------------------------------- work split
+// Units u = tile * S + segment; CTA c owns [c * total / G, (c + 1) * total / G).
+
+__host__ __device__ __forceinline__ int share_begin(int c, int total, int G) {
+  return static_cast<int>(static_cast<long long>(c) * total / G);
 }
-
-// EXL2 half step of width B: A = the word row of the lane's block (chunks
-// 2hf, 2hf + 1), Bn = the next word row when the block spills over
-template <int B, int MT>
-__device__ __forceinline__ void exl2_half(const uint4& A0, const uint4& A1, const uint4& B0, const uint4& B1,
-                                          const uint4& sc, uint32_t off, const uint4& xb0, const uint4& xb1,
-                                          float (&acc)[MT][4][4]) {
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    uint32_t P[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = 2 * nt + h;
-      const uint32_t wa = comp(c < 4 ? A0 : A1, c & 3);
-      uint32_t lo = wa, hi = 0;
-      if constexpr (B == 3 || B == 5 || B == 6) {
-        const uint32_t wb = comp(c < 4 ? B0 : B1, c & 3);
-        lo = fshr(wa, wb, off);
-        hi = wb >> off;
-      } else if constexpr (B == 2) {
-        lo = wa >> off;
-      } else if constexpr (B == 8) {
-        hi = comp(c < 4 ? B0 : B1, c & 3);
-      }
-      unpack8<B>(lo, hi, P[h]);
-      const uint32_t s2 = scale_x2(sc, c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) P[h][i] = hmul2(P[h][i], s2);  // w = fp16_RN((q - z) s)
-    }
-    mma_pair<MT>(acc, nt, P[0], P[1], xb0, xb1);
-  }
+// the CTA that owns unit u
+__host__ __device__ __forceinline__ int share_owner(int u, int total, int G) {
+  return static_cast<int>((static_cast<long long>(u + 1) * G - 1) / total);
 }
-
-// GPTQ half step: exact fp16 (q - z), scaled once: w = fp16_RN((q - z) s);
-// zlo / zhi / s2 point at the half's 8 column constants
-template <int MT>
-__device__ __forceinline__ void gptq_half(const uint4& A0, const uint4& A1, const uint32_t* zlo, const uint32_t* zhi,
-                                          const uint32_t* s2, const uint4& xb0, const uint4& xb1,
-                                          float (&acc)[MT][4][4]) {
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    uint32_t P[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int c = 2 * nt + h;
-      unpack8_gptq(comp(c < 4 ? A0 : A1, c & 3), zlo[c], zhi[c], P[h]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) P[h][i] = hmul2(P[h][i], s2[c]);
-    }
-    mma_pair<MT>(acc, nt, P[0], P[1], xb0, xb1);
-  }
-}
-
-__device__ __forceinline__ uint4 ld16(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ uint2 ld8(const uint8_t* p) { return *reinterpret_cast<const uint2*>(p); }
-__device__ __forceinline__ uint32_t ld4(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
-// ---------------------------------------------------------------- the kernel
-
-// Fetch side of one warp: walks the CTA's pieces and, inside each, the warp's
-// step range, P - 1 steps ahead of the math.
-struct Fetch {
-  int p;          // position of the next piece in the CTA's share
-  int s, ws, we;  // next step to fetch and its range
-  int tile;
-  bool live;      // a step remains to fetch
-};
 
 // Act-order gather: xp[m][j] = x[m][perm[j]] (stored-row order), one element
 // per thread so that many loads are in flight. Out-of-range entries read as 0
@@ -320,290 +331,314 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restric
   xp[e] = ok ? __ldg(x + static_cast<size_t>(e / K) * K + p) : static_cast<uint16_t>(0);
 }
 
-template <int FMT, int MODE>
-__global__ void __launch_bounds__(warps_of(MODE) * 32, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
-  constexpr int NW = warps_of(MODE);
-  constexpr int NT = NW * 32;
-  constexpr int MT = MODE == 1 ? 2 : 1;
-  constexpr int KG = NW / kCG;  // K groups
+__device__ __forceinline__ bool valid_width(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 
+// ---------------------------------------------------------------- the kernel
+// MT: 8-token blocks (1 for M <= 8, 2 for M <= 16).
+
+template <int FMT, int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* slots = smem;  // [kP][NT][kSlotBytes]
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + a.off_flags);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + a.off_x);
-  uint32_t* meta = reinterpret_cast<uint32_t*>(smem + a.off_meta);
-  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  // aligned by pointer arithmetic on the shared array, so that every access
+  // through it stays a shared-memory access
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+  uint64_t* empty = full + kMaxStages;
+  Desc* desc = reinterpret_cast<Desc*>(empty + kMaxStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(desc + kMaxStages);
+  int* pend = const_cast<int*>(abort_flag) + 4;           // [kMaxStages] x copies held back (producer)
+  uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + a.off_bar + 512);  // EXL2 segment offsets [S + 1]
 
-  const int tid = threadIdx.x;
-  const int w = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int cgi = w % kCG, kg = w / kCG;  // the warp's 64-column group and K group
-
-  Split sp;
-  sp.total = a.total;
-  sp.G = static_cast<int>(gridDim.x);
-  sp.n_tiles = a.n_tiles;
-  sp.n_steps = a.n_steps;
-  sp.kc_steps = a.kc_steps;
-  sp.n_chunks = a.n_chunks;
-  const int cta = blockIdx.x;
-  const int p_begin = sp.begin(cta), p_end = sp.begin(cta + 1);
-  const uint32_t nwr = static_cast<uint32_t>(a.n_word_rows);
-
-  // EXL2 step table of the staged chunk: word-row offset | width << 24, or 0
-  // for a width outside {2,3,4,5,6,8} or past the end of qweight
-  int st_lo = 0, st_hi = 0;
-  auto pack_step = [&](uint32_t o, uint32_t e) -> uint32_t {
-    o = min(o, nwr);
-    e = min(e, nwr);
-    const int b = static_cast<int>(e) - static_cast<int>(o);
-    const bool ok = b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8;
-    return ok ? (o | (static_cast<uint32_t>(b) << 24)) : 0u;
-  };
-  auto step_of = [&](int s) -> uint32_t {
-    if (s >= st_lo && s < st_hi) return meta[s - st_lo];
-    return pack_step(__ldg(a.seg_off + s), __ldg(a.seg_off + s + 1));
-  };
-  auto stage_meta = [&](int kc) {
-    st_lo = kc * a.kc_steps;
-    st_hi = st_lo + sp.chunk_len(kc);
-    if constexpr (FMT == EXQ_FMT_EXL2) {
-      for (int i = tid; i < st_hi - st_lo; i += NT)
-        meta[i] = pack_step(__ldg(a.seg_off + st_lo + i), __ldg(a.seg_off + st_lo + i + 1));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kConsumerWarps);  // every consumer warp reads every stage
     }
-  };
-
-  // ---- fetch side: one commit group per step, P - 1 steps ahead
-  Fetch fs;
-  fs.p = p_begin;
-  fs.live = false;
-  auto fetch_next_range = [&]() {
-    fs.live = false;
-    while (fs.p < p_end) {
-      int next;
-      const Piece pc = piece_at(sp, cta, fs.p, p_end, next);
-      fs.p = next;
-      int ws, we;
-      warp_range<KG>(pc, kg, ws, we);
-      if (ws < we) {
-        fs.s = fs.ws = ws;
-        fs.we = we;
-        fs.tile = pc.tile;
-        fs.live = true;
-        return;
-      }
-    }
-  };
-  const uint32_t slot0 = smem_u32(slots) + static_cast<uint32_t>(tid * kSlotBytes);
-  int iq = 0;  // steps fetched (including empty groups)
-  auto fetch = [&]() {
-    if (fs.live) {
-      const int s = fs.s;
-      const int col = fs.tile * kTN + 64 * cgi + 4 * g;
-      const bool hi_ok = col + 32 < a.N;  // N % 8 == 0: a 4-column chunk is all in or all out
-      const uint32_t dst = slot0 + static_cast<uint32_t>((iq % kP) * NT * kSlotBytes);
-      if (col < a.N) {
-        if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          const uint32_t* src = a.qweight + static_cast<size_t>(4 * s + t) * a.N + col;
-          cp_async16(dst, src);
-          if (hi_ok) cp_async16(dst + 16, src + 32);
-          if (s == fs.ws || s % a.gs_steps == 0) {  // scales and zeros once per group
-            const int grp = s / a.gs_steps;
-            const uint16_t* sp_ = a.scales + static_cast<size_t>(grp) * a.N + col;
-            const uint32_t* zp = a.qzeros + static_cast<size_t>(grp) * (a.N / 8) + col / 8;
-            cp_async8(dst + 64, sp_);
-            cp_async4(dst + 32, zp);
-            if (hi_ok) {
-              cp_async8(dst + 72, sp_ + 32);
-              cp_async4(dst + 36, zp + 4);
-            }
-          }
-        } else {
-          const uint32_t md = step_of(s);
-          const int b = static_cast<int>(md >> 24);
-          if (b != 0) {
-            int wi, off;
-            block_window(b, t, wi, off);
-            const uint32_t* src = a.qweight + static_cast<size_t>((md & 0xFFFFFFu) + wi) * a.N + col;
-            const uint16_t* sp_ = a.scales + static_cast<size_t>(s) * a.N + col;
-            const bool second = b == 8 || ((b == 3 || b == 5 || b == 6) && block_needs_second(b, off));
-            cp_async16(dst, src);
-            if (second) cp_async16(dst + 32, src + a.N);
-            cp_async8(dst + 64, sp_);
-            if (hi_ok) {
-              cp_async16(dst + 16, src + 32);
-              if (second) cp_async16(dst + 48, src + a.N + 32);
-              cp_async8(dst + 72, sp_ + 32);
-            }
-          }
-        }
-      }
-      if (++fs.s == fs.we) fetch_next_range();
-    }
-    cp_async_commit();  // one group per call, possibly empty, keeps the count uniform
-    ++iq;
-  };
-
-  // ---- staging of x (already in stored-row order), each 8-row block as
-  // (x0,x4),(x1,x5),(x2,x6),(x3,x7)
-  int next0 = 0;
-  const int kc0 = p_begin < p_end ? piece_at(sp, cta, p_begin, p_end, next0).kc : 0;
-  auto stage_x = [&](int kc) {
-    const int c0 = kc * a.kc_steps;
-    const int blocks = sp.chunk_len(kc) * 4;
-    const int xtotal = a.M * blocks;
-    for (int e = tid; e < xtotal; e += NT) {
-      const int m = e / blocks, blk = e - m * blocks;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(m) * a.K + c0 * 32 + blk * 8));
-      uint4 o;
-      o.x = prmt(v.x, v.z, 0x5410);
-      o.y = prmt(v.x, v.z, 0x7632);
-      o.z = prmt(v.y, v.w, 0x5410);
-      o.w = prmt(v.y, v.w, 0x7632);
-      *reinterpret_cast<uint4*>(xs + m * a.xs_stride + blk * 8) = o;
-    }
-  };
-
-  // weights, scales and offsets are model state: start fetching before the
-  // wait for the previous kernel
-  if (tid == 0) *last_flag = 0;
-  stage_meta(kc0);
-  __syncthreads();
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  fetch_next_range();
-#pragma unroll
-  for (int i = 0; i < kP - 1; ++i) fetch();
+  __syncthreads();
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  int staged = kc0;
-  if (p_begin < p_end) stage_x(kc0);
-  cta_barrier<NW>();
+  const int G = static_cast<int>(gridDim.x);
+  const int u0 = share_begin(blockIdx.x, a.total, G), u1 = share_begin(blockIdx.x + 1, a.total, G);
 
-  int cq = 0;  // steps consumed
-  float acc[MT][4][4];
-  const uint16_t* xr0 = xs + g * a.xs_stride + 8 * t;
-  const uint16_t* xr1 = xs + (g + 8) * a.xs_stride + 8 * t;
-  const bool x0_ok = g < a.M, x1_ok = MT == 2 && g + 8 < a.M;
-  const uint8_t* myslot = slots + tid * kSlotBytes;
-
-  int p = p_begin, next = p_begin;
-  while (p < p_end) {
-    const Piece pc = piece_at(sp, cta, p, p_end, next);
-    p = next;
-    if (pc.kc != staged) {
-      cta_barrier<NW>();
-      stage_meta(pc.kc);
-      stage_x(pc.kc);
-      cta_barrier<NW>();
-      staged = pc.kc;
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.s)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
     }
-    const int c0 = pc.kc * a.kc_steps;
-    zero_acc<MT>(acc);
-    int ws, we;
-    warp_range<KG>(pc, kg, ws, we);
-
-    uint32_t zlo[8], zhi[8], s2[8];  // GPTQ: the current group's column constants
-    for (int s = ws; s < we; ++s) {
-      fetch();
-      cp_async_wait<kP - 1>();  // this lane's copies of step s have landed
-      const uint8_t* sl = myslot + (cq % kP) * NT * kSlotBytes;
-      ++cq;
-      const int kl = (s - c0) * 32;
-      const uint4 zero4 = make_uint4(0, 0, 0, 0);
-      const uint4 xb0 = x0_ok ? *reinterpret_cast<const uint4*>(xr0 + kl) : zero4;
-      const uint4 xb1 = x1_ok ? *reinterpret_cast<const uint4*>(xr1 + kl) : zero4;
+    if constexpr (FMT == EXQ_FMT_EXL2) {
+      // the segment table is model state: copy it before the wait
+      for (int i = lane; i <= a.S; i += 32) cp_async4(smem_u32(tbl + i), a.seg_off + i);
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncwarp();
+    }
+    const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXRowBytes;
+    const uint32_t tx = kRowsPerStage * kTN * 4 + kScaleRows * kTN * 2 + x_bytes;
+    int slot = 0, ephase = 0, issued = 0, npend = 0;
+    bool waited = false, ok = true;
+    auto release_x = [&]() {  // the activations may be read once the previous kernel is done
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (lane == 0)
+        for (int i = 0; i < npend; ++i) {
+          const int sl = pend[i] & 0xFF, seg = pend[i] >> 8;
+          tma_load_2d(smem_u32(smem + sl * a.slot_bytes + kSlotX), &maps.x, seg * 32, 0, smem_u32(&full[sl]));
+        }
+      npend = 0;
+      waited = true;
+    };
+    // one stage into the next slot; false once a wait gave up
+    auto issue = [&](uint32_t da, uint32_t widths, int tile, int row0, int srow, bool bad) -> bool {
+      if (!waited && issued >= a.stages) release_x();  // the ring is about to wrap
+      if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag)) return false;
+      uint8_t* st = smem + slot * a.slot_bytes;
+      const uint32_t fb = smem_u32(&full[slot]);
+      if (lane == 0) desc[slot] = Desc{da, widths, static_cast<uint32_t>(tile), static_cast<uint32_t>(srow)};
       if constexpr (FMT == EXQ_FMT_GPTQ4) {
-        if (s == ws || s % a.gs_steps == 0) {  // first step of the warp's part of a group
-          const uint32_t zsh = 16u * (g & 1);
-          const uint32_t z0 = ld4(sl + 32) >> zsh, z1 = ld4(sl + 36) >> zsh;
+        if (!bad) {
+          const int nz = a.N / 8, cw = tile * (kTN / 8) + lane;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) gptq_zero_consts(((c < 4 ? z0 : z1) >> (4 * (c & 3))) & 0xFu, zlo[c], zhi[c]);
-          const uint2 q0 = ld8(sl + 64), q1 = ld8(sl + 72);
-          const uint4 sv = make_uint4(q0.x, q0.y, q1.x, q1.y);
+          for (int r = 0; r < kScaleRows; ++r)
+            if (srow + r < a.G && cw < nz && lane < kTN / 8)
+              cp_async4(smem_u32(st + kSlotZ + r * kZeroRowBytes + lane * 4),
+                        a.qzeros + static_cast<size_t>(srow + r) * nz + cw);
+          cp_async_arrive(fb);  // one more pending arrival, made when this lane's copies land
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (bad) {
+          mbar_arrive(fb);
+        } else {
+          mbar_expect_tx(fb, tx);
+          tma_load_2d(smem_u32(st + kSlotW), &maps.w, tile * kTN, row0, fb);
+          tma_load_2d(smem_u32(st + kSlotS), &maps.s, tile * kTN, srow, fb);
+          if (waited) tma_load_2d(smem_u32(st + kSlotX), &maps.x, static_cast<int>(da & 0xFFFFu) * 32, 0, fb);
+        }
+      }
+      if (!bad && !waited) pend[npend++] = slot | (static_cast<int>(da & 0xFFFFu) << 8);
+      ++issued;
+      if (++slot == a.stages) {
+        slot = 0;
+        ephase ^= 1;
+      }
+      return true;
+    };
+
+    for (int u = u0; u < u1 && ok;) {
+      const int tile = u / a.S;
+      const int sa = u - tile * a.S;
+      const int sb = min(a.S, sa + (u1 - u));
+      u += sb - sa;
+      bool first = true;
+      for (int seg = sa; seg < sb && ok;) {
+        int n, row0, srow;
+        uint32_t widths = 0;
+        int ps_h = 0;  // EXL2: this lane's inclusive prefix sum of the stage's widths
+        bool bad = false;
+        if constexpr (FMT == EXQ_FMT_GPTQ4) {
+          n = min(sb, (seg / kSegsPerStage + 1) * kSegsPerStage) - seg;
+          row0 = 4 * seg;
+          srow = seg / a.gs_seg;
+        } else {
+          // greedy, one candidate segment per lane: the longest run of valid
+          // segments from seg (at most four) whose widths add up to at most 16
+          const int sk = seg + lane;
+          const bool cand = lane < kSegsPerStage && sk < sb;
+          const uint32_t e0 = cand ? tbl[sk] : 0u, e1 = cand ? tbl[sk + 1] : 0u;
+          const int b = static_cast<int>(e1) - static_cast<int>(e0);
+          const bool good = cand && valid_width(b) && e1 <= static_cast<uint32_t>(a.n_word_rows);
+          int ps = good ? b : 0;  // inclusive prefix sum of the widths over lanes 0..7
 #pragma unroll
-          for (int c = 0; c < 8; ++c) s2[c] = scale_x2(sv, c);
+          for (int d = 1; d < 8; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, ps, d);
+            if (lane >= d) ps += v;
+          }
+          const unsigned stop = __ballot_sync(0xffffffffu, !(good && ps <= kRowsPerStage));
+          n = __ffs(stop) - 1;  // leading lanes that fit (stop always has a bit at or below lane 4)
+          widths = __reduce_or_sync(0xffffffffu, lane < n ? static_cast<uint32_t>(b) << (4 * lane) : 0u);
+          ps_h = ps;
+          row0 = static_cast<int>(__shfl_sync(0xffffffffu, e0, 0));
+          srow = seg;
+          if (n == 0) {  // the segment at seg itself is malformed: skip it alone, reported
+            bad = true;
+            n = 1;
+            if (lane == 0) atomicOr(&g_gemv_err, kDevErrBadSegment);
+          }
         }
-        gptq_half<MT>(ld16(sl), ld16(sl + 16), zlo, zhi, s2, xb0, xb1, acc);
-      } else {
-        const uint32_t md = step_of(s);
-        const int b = static_cast<int>(md >> 24);
-        if (b == 0) {  // warp-uniform; nothing was fetched for it
-          if (lane == 0) atomicOr(&g_gemv_err, kDevErrBadSegment);
-          continue;
+        const bool last = seg + n == sb;
+        const int h = (n + 1) >> 1;  // segments of the first consumer K group
+        uint32_t half, db;
+        if constexpr (FMT == EXQ_FMT_GPTQ4) {
+          const int gh = (seg + h) / a.gs_seg;
+          half = static_cast<uint32_t>(gh - srow);
+          db = static_cast<uint32_t>(seg - srow * a.gs_seg) | (static_cast<uint32_t>(seg + h - gh * a.gs_seg) << 16);
+        } else {
+          half = static_cast<uint32_t>(__shfl_sync(0xffffffffu, ps_h, h - 1));
+          db = widths;
         }
-        int wi, off;
-        block_window(b, t, wi, off);
-        const uint4 A0 = ld16(sl), A1 = ld16(sl + 16);
-        const uint4 B0 = ld16(sl + 32), B1 = ld16(sl + 48);
-        const uint2 q0 = ld8(sl + 64), q1 = ld8(sl + 72);
-        const uint4 sc = make_uint4(q0.x, q0.y, q1.x, q1.y);
-        switch (b) {
-          case 2: exl2_half<2, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
-          case 3: exl2_half<3, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
-          case 4: exl2_half<4, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
-          case 5: exl2_half<5, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
-          case 6: exl2_half<6, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
-          default: exl2_half<8, MT>(A0, A1, B0, B1, sc, off, xb0, xb1, acc); break;
+        const uint32_t da = static_cast<uint32_t>(seg) | (static_cast<uint32_t>(n) << 16) | (first ? kDescFirst : 0u) |
+                            (last ? kDescLast : 0u) | (half << 24);
+        ok = issue(da, db, tile, row0, srow, bad);
+        seg += n;
+        first = false;
+      }
+    }
+    if (!waited) release_x();
+    const bool ended = ok && warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag);
+    if (ended && lane == 0) {
+      desc[slot] = Desc{kDescEnd, 0u, 0u, 0u};
+      mbar_arrive(smem_u32(&full[slot]));
+    }
+    // after a give-up no consumer will wait for the copies still in flight:
+    // they land before the CTA may exit (otherwise the consumers saw them all)
+    if (!ended && lane == 0)
+      for (int i = max(0, issued - a.stages); i < issued; ++i) {
+        const uint32_t bar = smem_u32(&full[i % a.stages]);
+        for (long long r = 0; r < kWaitLimit; ++r)
+          if (mbar_try_wait(bar, (i / a.stages) & 1)) break;
+      }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // y and the workspace are shared with earlier kernels
+  const int g = lane >> 2, t = lane & 3;
+  const int w = warp & (kColGroups - 1);  // column group: columns 32w .. 32w+31 of the tile
+  const int kg = warp / kColGroups;       // K group: the stage's segments j with j % 2 == kg
+  const int tok[2] = {min(g, a.M - 1), min(g + 8, a.M - 1)};
+  float acc[MT][2][4];
+  zero4<MT>(acc);
+  uint32_t zlo[4] = {0u, 0u, 0u, 0u}, zhi[4] = {0u, 0u, 0u, 0u}, s2[4] = {0u, 0u, 0u, 0u};
+  int slot = 0, fphase = 0;
+  for (;;) {
+    if (!warp_wait(smem_u32(&full[slot]), fphase, abort_flag)) break;
+    const Desc d = desc[slot];
+    if (d.a & kDescEnd) break;
+    const uint8_t* sl = smem + slot * a.slot_bytes;
+    const int seg0 = static_cast<int>(d.a & 0xFFFFu), n = static_cast<int>((d.a >> 16) & 15u);
+    if (d.a & kDescFirst) zero4<MT>(acc);
+    const uint8_t* wrow = sl + kSlotW + 128 * w + 16 * g;
+    const uint8_t* xrow0 = sl + kSlotX + tok[0] * kXRowBytes + 16 * t;
+    const uint8_t* xrow1 = sl + kSlotX + tok[1] * kXRowBytes + 16 * t;
+    const int col_off = 64 * w + 8 * g;  // byte offset of the lane's 4 scales in a scale row
+    const int h = (n + 1) >> 1;
+    const int j0 = kg ? h : 0, j1 = kg ? n : h;  // this K group's segments of the stage
+    if constexpr (FMT == EXQ_FMT_EXL2) {
+      const uint32_t widths = d.b;
+      int o = kg ? static_cast<int>(d.a >> 24) : 0;  // word row of segment j0 in the slot
+      for (int j = j0; j < j1; ++j) {
+        const int b = static_cast<int>((widths >> (4 * j)) & 15u);
+        if (b != 0) {  // 0: a segment the producer rejected (reported)
+          uint32_t xb[MT][4];
+          x_pairs(xrow0 + 64 * j, xb[0]);
+          if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+          scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
+          const int bit = 8 * t * b;
+          const uint8_t* row = wrow + (o + (bit >> 5)) * kRowBytes;
+          const uint32_t off = static_cast<uint32_t>(bit & 31);
+          switch (b) {
+            case 2: exl2_seg<2, MT>(row, off, xb, s2, acc); break;
+            case 3: exl2_seg<3, MT>(row, off, xb, s2, acc); break;
+            case 4: exl2_seg<4, MT>(row, off, xb, s2, acc); break;
+            case 5: exl2_seg<5, MT>(row, off, xb, s2, acc); break;
+            case 6: exl2_seg<6, MT>(row, off, xb, s2, acc); break;
+            default: exl2_seg<8, MT>(row, off, xb, s2, acc); break;
+          }
+        }
+        o += b;
+      }
+    } else {
+      int rem = static_cast<int>(kg ? (d.b >> 16) : (d.b & 0xFFFFu));  // position of segment j0 in its group
+      int r = kg ? static_cast<int>(d.a >> 24) : 0;                       // its scale / zero row in the slot
+      int loaded = -1;  // the row whose zeros and scales are in registers
+      for (int j = j0; j < j1; ++j) {
+        if (r != loaded) {  // this warp's first segment of the slot, or a new group
+          loaded = r;
+          const uint32_t zw = lds32(sl + kSlotZ + r * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) gptq_zero_consts((zw >> (4 * c)) & 0xFu, zlo[c], zhi[c]);
+          scales4(sl + kSlotS + r * (kTN * 2) + col_off, s2);
+        }
+        uint32_t xb[MT][4];
+        x_pairs(xrow0 + 64 * j, xb[0]);
+        if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+        const uint4 wq = lds128(wrow + (4 * j + t) * kRowBytes);
+        uint32_t P[4][4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) unpack8_gptq(comp(wq, c), zlo[c], zhi[c], P[c]);
+        scale_pairs(P, s2);
+        seg_mma<MT>(acc, P, xb);
+        if (++rem == a.gs_seg) {
+          rem = 0;
+          ++r;
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    if (++slot == a.stages) {
+      slot = 0;
+      fphase ^= 1;
+    }
 
-    // ---- the piece's sums: K groups added in order, then y or the workspace
-    const int elems = a.M * kTN;
-    {
-      float* rw = red + w * a.M * 64;  // [NW][M][64]
+    if (d.a & kDescLast) {
+      // ---- this warp's share of the piece: 32 columns, one K group. Every
+      // (piece, K group) leaves fp32 partial sums; the last of the tile's
+      // 2P arrivals at the column group's counter adds them in order.
+      const int tile = static_cast<int>(d.c);
+      const int first = share_owner(tile * a.S, a.total, G);
+      const int P2 = 2 * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
+      const int pslot = 2 * (static_cast<int>(blockIdx.x) - first) + kg;
+      float* part = a.partials + (static_cast<size_t>(tile) * a.max_pieces + pslot) * a.M * kTP;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = 8 * mt + 2 * t + (i & 1);
-            if (m < a.M) rw[m * 64 + group_col(2 * nt + (i >> 1), g)] = acc[mt][nt][i];
-          }
-    }
-    cta_barrier<NW>();
-    // element e = m * kTN + c of the tile: column group c / 64, K groups kg
-    auto tile_sum = [&](int e) {
-      const int m = e / kTN, c = e - m * kTN;
-      float v = 0.f;
-      for (int k = 0; k < KG; ++k) v += red[((k * kCG + c / 64) * a.M + m) * 64 + (c & 63)];
-      return v;
-    };
-    const int n0 = pc.tile * kTN;
-    if (pc.P == 1) {
-      for (int e = tid; e < elems; e += NT) {
-        const float v = tile_sum(e);
-        const int n = n0 + (e % kTN);
-        if (n < a.N) a.y[static_cast<size_t>(e / kTN) * a.N + n] = __half_as_ushort(__float2half_rn(v));
-      }
-    } else {
-      float* part = a.partials + (static_cast<size_t>(pc.tile) * a.max_pieces + pc.slot) * elems;
-      for (int e = tid; e < elems; e += NT) part[e] = tile_sum(e);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int m = 8 * mt + 2 * t + hh;
+          if (m < a.M)
+            *reinterpret_cast<float4*>(part + m * kTP + 32 * w + 4 * g) =
+                make_float4(acc[mt][0][hh], acc[mt][0][2 + hh], acc[mt][1][hh], acc[mt][1][2 + hh]);
+        }
       __threadfence();
-      cta_barrier<NW>();
-      if (tid == 0) {
-        const unsigned old = atomicAdd(&a.counters[pc.tile], 1u);
-        const int last = old == static_cast<unsigned>(pc.P - 1);
-        if (last) atomicExch(&a.counters[pc.tile], 0u);  // ready for the next call
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        unsigned* ctr = a.counters + tile * kColGroups + w;
+        const unsigned old = atomicAdd(ctr, 1u);
+        last = old == static_cast<unsigned>(P2 - 1);
+        if (last) atomicExch(ctr, 0u);  // ready for the next call
         __threadfence();
-        *last_flag = last;
       }
-      cta_barrier<NW>();
-      if (*last_flag) {
-        const float* base = a.partials + static_cast<size_t>(pc.tile) * a.max_pieces * elems;
-        for (int e = tid; e < elems; e += NT) {
+      last = __shfl_sync(0xffffffffu, last, 0);
+      __syncwarp();
+      if (last) {
+        const float* base = a.partials + static_cast<size_t>(tile) * a.max_pieces * a.M * kTP + 32 * w + lane;
+        const int n = tile * kTN + 32 * w + lane;
+        const bool n_ok = 32 * w + lane < kTN && n < a.N;
+        const size_t stride = static_cast<size_t>(a.M) * kTP;
+        for (int m = 0; m < a.M; ++m) {
+          // pieces added in piece order, 32 loads in flight at a time
+          const float* pm = base + static_cast<size_t>(m) * kTP;
           float v = 0.f;
-          for (int k = 0; k < pc.P; ++k) v += __ldcg(base + static_cast<size_t>(k) * elems + e);
-          const int n = n0 + (e % kTN);
-          if (n < a.N) a.y[static_cast<size_t>(e / kTN) * a.N + n] = __half_as_ushort(__float2half_rn(v));
+          for (int p0 = 0; p0 < P2; p0 += 32) {
+            float q[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) q[i] = p0 + i < P2 ? __ldcg(pm + (p0 + i) * stride) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v += q[i];
+          }
+          if (n_ok) a.y[static_cast<size_t>(m) * a.N + n] = __half_as_ushort(__float2half_rn(v));
         }
       }
     }
-    cta_barrier<NW>();  // red and last_flag are rewritten by the next piece
   }
-  cp_async_wait<0>();
 }
 
 }  // namespace
@@ -614,88 +649,61 @@ __global__ void __launch_bounds__(warps_of(MODE) * 32, 1) gemv_kernel(const __gr
 namespace exq {
 namespace {
 
-using KernelFn = void (*)(GemvArgs);
+using KernelFn = void (*)(GemvMaps, GemvArgs);
 
 template <int FMT>
 KernelFn pick_for(int M) {
-  return mode_for(M) == 0 ? gemv_kernel<FMT, 0> : gemv_kernel<FMT, 1>;
+  return M <= 8 ? gemv_kernel<FMT, 1> : gemv_kernel<FMT, 2>;
 }
 
 KernelFn pick_kernel(int fmt, int M) {
   return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4>(M) : pick_for<EXQ_FMT_EXL2>(M);
 }
 
+int variant_index(int fmt, int M) { return (fmt == EXQ_FMT_GPTQ4 ? 0 : 2) + (M <= 8 ? 0 : 1); }
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-int xs_stride_for(int k_len) {
-  // token rows an odd multiple of 64 bytes apart: the quarter-warp of an
-  // LDS.128 (two token rows x four 16-byte blocks) touches distinct banks
-  return (k_len % 64 == 32) ? k_len : k_len + 32;
-}
+constexpr int kSmemPerCta = 210 * 1024;  // one CTA per SM
 
 struct Plan {
-  int G, NW, n_tiles, n_steps, kc_steps, n_chunks, max_pieces, xs_stride;
-  int total;
-  int off_flags, off_x, off_meta, off_red;
-  size_t smem;          // dynamic shared memory bytes (with the alignment slack)
-  size_t ws_counters;   // bytes of the counter region (256-aligned)
-  size_t ws_partials;   // bytes of the partial sums
-  size_t ws_bytes;      // workspace bytes (+ M * K * 2 for a permuted layer's gathered x)
+  int G, S, n_tiles, total, max_pieces, stages, slot_bytes, off_bar;
+  size_t smem;         // dynamic shared memory bytes (with the alignment slack)
+  size_t ws_partials;  // bytes of the partial sums
+  size_t ws_bytes;     // counters + partials (+ M * K * 2 for a permuted layer's gathered x)
 };
 
-// Layout of one launch on a device with `sm_count` SMs; false if it cannot fit.
-bool make_plan(int K, int N, int M, bool perm, int sm_count, int smem_max, Plan& p) {
-  p.n_steps = K / 32;
-  p.n_tiles = (N + kTN - 1) / kTN;
-  const long long total = static_cast<long long>(p.n_tiles) * p.n_steps;
+// Layout of one launch on a device with `sm_count` SMs; false if this
+// kernel cannot take the layer.
+bool make_plan(const exq_weight& w, int M, int sm_count, Plan& p) {
+  if (M < 1 || M > 16) return false;
+  p.S = w.K / 32;
+  if (p.S > 0xFFFF) return false;  // segment indices travel in 16 bits
+  p.n_tiles = (w.N + kTN - 1) / kTN;
+  if (p.n_tiles * kColGroups * 4 > kCounterBytes) return false;
+  const long long total = static_cast<long long>(p.n_tiles) * p.S;
   if (total >= (1ll << 31)) return false;
   p.total = static_cast<int>(total);
-  const int mode = mode_for(M);
-  p.NW = warps_of(mode);
   int G = sm_count;
-  if (const char* env = std::getenv("EXQ_GEMV_CTAS")) {  // CTA-count override for tuning sweeps
+  if (const char* env = std::getenv("EXQ_GEMV_CTAS")) {  // CTA-count override for tests of the split
     const int v = std::atoi(env);
     if (v > 0) G = v;
   }
-  p.G = std::min(G, p.total);
-
-  size_t off = 0;
-  off += static_cast<size_t>(kP) * p.NW * 32 * kSlotBytes;
-  p.off_flags = static_cast<int>(off);
-  off += 128;
-  p.off_red = static_cast<int>(off);
-  off += static_cast<size_t>(p.NW) * M * 64 * 4;
-  const size_t fixed = off + 1024;  // + slack to align the dynamic base to 1024
-  if (fixed >= static_cast<size_t>(smem_max)) return false;
-  // x costs M * 64 bytes per step (+ one 64-byte pad per token row), the
-  // EXL2 offsets 4 bytes per step (+ 1 entry)
-  const long long budget = static_cast<long long>(smem_max) - static_cast<long long>(fixed) - 64LL * M - 64;
-  const long long per_step = 64LL * M + 4;
-  long long kc = budget / per_step;
-  if (kc < 1) return false;
-  kc = std::min<long long>(kc, p.n_steps);
-  p.n_chunks = static_cast<int>((p.n_steps + kc - 1) / kc);
-  p.kc_steps = (p.n_steps + p.n_chunks - 1) / p.n_chunks;  // even chunks
-  p.xs_stride = xs_stride_for(p.kc_steps * 32);
-  p.off_x = static_cast<int>(off);
-  off += align_up(static_cast<size_t>(M) * p.xs_stride * 2, 16);
-  p.off_meta = static_cast<int>(off);
-  off += align_up(static_cast<size_t>(p.kc_steps + 1) * 4, 16);
-  p.smem = off + 1024;
-  if (p.smem > static_cast<size_t>(smem_max)) return false;
-
-  // pieces per tile: a unit of len positions meets at most (len - 1) / s + 2
-  // shares when every share holds at least s positions
-  const int min_share = p.total / p.G;
-  p.max_pieces = 0;
-  for (int kc_i = 0; kc_i < p.n_chunks; ++kc_i) {
-    const int len = kc_i == p.n_chunks - 1 ? p.n_steps - kc_i * p.kc_steps : p.kc_steps;
-    p.max_pieces += static_cast<int>((len - 1) / min_share) + 2;
-  }
-  if (p.n_tiles * 4 > kCounterBytes) return false;
-  p.ws_counters = kCounterBytes;  // a fixed region: no call's scratch ever lands on another's counters
-  p.ws_partials = align_up(static_cast<size_t>(p.n_tiles) * p.max_pieces * M * kTN * 4, 256);
-  p.ws_bytes = p.ws_counters + p.ws_partials + (perm ? align_up(static_cast<size_t>(M) * K * 2, 256) : 0);
+  p.G = std::max(1, std::min(G, p.total));
+  p.slot_bytes = slot_bytes_for(M);
+  const size_t table = w.format == EXQ_FMT_EXL2 ? align_up(static_cast<size_t>(p.S + 1) * 4, 16) : 0;
+  const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment table, alignment slack
+  const long long room = static_cast<long long>(kSmemPerCta) - static_cast<long long>(fixed);
+  p.stages = static_cast<int>(std::min<long long>(kMaxStages, room / p.slot_bytes));
+  if (p.stages < 2) return false;
+  p.off_bar = p.stages * p.slot_bytes;
+  p.smem = static_cast<size_t>(p.off_bar) + fixed;
+  // a tile of S units meets at most (S - 1) / s + 2 shares of at least s
+  // units; each leaves one partial per K group
+  const int min_share = std::max(1, p.total / p.G);
+  p.max_pieces = 2 * std::min(p.G, (p.S - 1) / min_share + 2);
+  p.ws_partials = align_up(static_cast<size_t>(p.n_tiles) * p.max_pieces * M * kTP * 4, 256);
+  p.ws_bytes = kCounterBytes + p.ws_partials + (w.perm ? align_up(static_cast<size_t>(M) * w.K * 2, 256) : 0);
   return true;
 }
 
@@ -707,9 +715,8 @@ bool g_attr_done[64][4];
 size_t gemv_workspace_bytes(const exq_weight& w, int M) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  const DeviceInfo& di = device_info(dev);
   Plan plan{};
-  if (!make_plan(w.K, w.N, M, w.perm != nullptr, di.sm_count, di.max_smem_optin, plan)) return 0;
+  if (!make_plan(w, M, device_info(dev).sm_count, plan)) return 0;
   return plan.ws_bytes;
 }
 
@@ -721,18 +728,18 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   if (di.sm_count <= 0 || dev >= 64) return EXQ_ERR_CUDA;
 
   Plan plan{};
-  if (!make_plan(w.K, w.N, M, w.perm != nullptr, di.sm_count, di.max_smem_optin, plan)) return EXQ_ERR_UNSUPPORTED;
+  if (!make_plan(w, M, di.sm_count, plan)) return EXQ_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return EXQ_ERR_INVALID_ARG;
 
   KernelFn fn = pick_kernel(w.format, M);
-  const int fidx = (w.format == EXQ_FMT_GPTQ4 ? 0 : 2) + mode_for(M);
   {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (!g_attr_done[dev][fidx]) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin) != cudaSuccess)
+    bool& done = g_attr_done[dev][variant_index(w.format, M)];
+    if (!done) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess)
         return EXQ_ERR_CUDA;
-      g_attr_done[dev][fidx] = true;
+      done = true;
     }
   }
 
@@ -745,11 +752,11 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     ++na;
   }
 
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   // act-order: gather x into stored-row order once, into the workspace
   const uint16_t* xs_src = x;
   if (w.perm) {
-    uint16_t* xp = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + plan.ws_counters +
-                                               plan.ws_partials);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(ws + kCounterBytes + plan.ws_partials);
     const int threads = M * w.K;
     cudaLaunchConfig_t gcfg{};
     gcfg.gridDim = dim3((threads + 255) / 256, 1, 1);
@@ -764,40 +771,45 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     xs_src = xp;
   }
 
+  GemvMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const int scale_rows = w.format == EXQ_FMT_GPTQ4 ? w.n_groups : w.K / 32;
+  if (!encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.qweight, w.N, w.n_word_rows,
+                 static_cast<uint64_t>(w.N) * 4, kTN, kRowsPerStage) ||
+      !encode_2d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, w.scales, w.N, scale_rows, static_cast<uint64_t>(w.N) * 2,
+                 kTN, kScaleRows) ||
+      !encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xs_src, w.K, M, static_cast<uint64_t>(w.K) * 2,
+                 kSegsPerStage * 32, M))
+    return EXQ_ERR_CUDA;
+
   GemvArgs args{};
-  args.qweight = w.qweight;
-  args.scales = w.scales;
-  args.qzeros = w.qzeros;
   args.seg_off = w.seg_word_off;
-  args.x = xs_src;
+  args.qzeros = w.qzeros;
   args.y = y;
-  args.counters = static_cast<uint32_t*>(workspace);
-  args.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.ws_counters);
+  args.counters = reinterpret_cast<uint32_t*>(ws);
+  args.partials = reinterpret_cast<float*>(ws + kCounterBytes);
   args.K = w.K;
   args.N = w.N;
   args.M = M;
-  args.n_steps = plan.n_steps;
-  args.gs_steps = w.format == EXQ_FMT_GPTQ4 ? w.group_size / 32 : 1;
+  args.S = plan.S;
+  args.gs_seg = w.format == EXQ_FMT_GPTQ4 ? w.group_size / 32 : 1;
+  args.G = w.format == EXQ_FMT_GPTQ4 ? w.n_groups : plan.S;
   args.n_word_rows = w.n_word_rows;
   args.n_tiles = plan.n_tiles;
-  args.kc_steps = plan.kc_steps;
-  args.n_chunks = plan.n_chunks;
-  args.max_pieces = plan.max_pieces;
-  args.xs_stride = plan.xs_stride;
   args.total = plan.total;
-  args.off_flags = plan.off_flags;
-  args.off_x = plan.off_x;
-  args.off_meta = plan.off_meta;
-  args.off_red = plan.off_red;
+  args.max_pieces = plan.max_pieces;
+  args.stages = plan.stages;
+  args.slot_bytes = plan.slot_bytes;
+  args.off_bar = plan.off_bar;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(plan.G, 1, 1);
-  cfg.blockDim = dim3(plan.NW * 32, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  if (cudaLaunchKernelEx(&cfg, fn, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, fn, maps, args) != cudaSuccess) {
     cudaGetLastError();
     return EXQ_ERR_CUDA;
   }

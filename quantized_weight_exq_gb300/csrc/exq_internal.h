@@ -2,6 +2,7 @@
 // kernel translation units. Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "exq.h"
@@ -23,6 +24,18 @@ struct DeviceInfo {
 
 // queried once per device, cached (host-only, thread-safe)
 const DeviceInfo& device_info(int device);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if absent)
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled tensor_map_encoder();
+
+// A 2-D tiled tensor map without swizzle: dims {inner, outer} elements, the
+// outer stride in bytes, box {box_inner, box_outer}; elements outside the
+// tensor read as zero. False if the driver rejects it.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);

@@ -200,11 +200,13 @@ def test_gemv_workspace_contract(env):
     with pytest.raises(exq.ExqError) as ei:
         exq.exq_gemv(w, x, y, workspace=short)
     assert ei.value.status == exq.EXQ_ERR_INVALID_ARG
-    # one workspace serves a run of calls with different layers and M
-    ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
-    for K, N, M in ((1024, 128, 1), (4096, 1024, 16), (2048, 264, 3)):
-        ee = exl2_case(K, N, seed=K + M)
-        ww = _exl2_dev(exq, ee)
+    # one workspace, as large as the largest call needs, serves a run of
+    # calls with different layers and M
+    runs = [(K, N, M, exl2_case(K, N, seed=K + M)) for K, N, M in ((1024, 128, 1), (4096, 1024, 16), (2048, 264, 3))]
+    devs = [_exl2_dev(exq, ee) for _, _, _, ee in runs]
+    ws = torch.zeros(max(exq.exq_gemv_workspace_size(ww, M) for (_, _, M, _), ww in zip(runs, devs)),
+                     dtype=torch.uint8, device="cuda")
+    for (K, N, M, ee), ww in zip(runs, devs):
         xx = synth.activations(M, K, seed=M)
         yy = torch.empty(M, N, dtype=torch.float16, device="cuda")
         exq.exq_gemv(ww, _x(torch, xx), yy, workspace=ws)

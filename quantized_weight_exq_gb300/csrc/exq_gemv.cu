@@ -316,11 +316,14 @@ __host__ __device__ __forceinline__ int share_owner(int u, int total, int G) {
 
 // Act-order gather: xp[m][j] = x[m][perm[j]] (stored-row order), one element
 // per thread so that many loads are in flight. Out-of-range entries read as 0
-// and are reported.
+// and are reported. It also pulls the EXL2 segment table (seg_off, S + 1
+// entries, or NULL) into L2 for the GEMV that follows.
 __global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                                       int M, int K, uint16_t* __restrict__ xp) {
+                                                       int M, int K, uint16_t* __restrict__ xp,
+                                                       const uint32_t* __restrict__ seg_off, int S) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (seg_off && e * 32 <= S) asm volatile("prefetch.global.L2 [%0];" ::"l"(seg_off + e * 32));
   const bool in = e < M * K;
   const int j = in ? e % K : 0;
   const int p = in ? __ldg(perm + j) : 0;  // the permutation is model state: read it before the wait
@@ -606,15 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(part + m * kTP + 32 * w + 4 * g) =
                 make_float4(acc[mt][0][hh], acc[mt][0][2 + hh], acc[mt][1][hh], acc[mt][1][2 + hh]);
         }
-      __threadfence();
+      // the warp's stores, then one acquire-release increment by lane 0: it
+      // publishes them and, for the last arriver, makes every other piece's
+      // stores visible to the reads below
       __syncwarp();
       int last = 0;
       if (lane == 0) {
         unsigned* ctr = a.counters + tile * kColGroups + w;
-        const unsigned old = atomicAdd(ctr, 1u);
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
         last = old == static_cast<unsigned>(P2 - 1);
         if (last) atomicExch(ctr, 0u);  // ready for the next call
-        __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       __syncwarp();
@@ -764,7 +769,8 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     gcfg.stream = stream;
     gcfg.attrs = attrs;
     gcfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&gcfg, gather_x_kernel, x, w.perm, M, w.K, xp) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&gcfg, gather_x_kernel, x, w.perm, M, w.K, xp, w.seg_word_off, w.K / 32) !=
+        cudaSuccess) {
       cudaGetLastError();
       return EXQ_ERR_CUDA;
     }

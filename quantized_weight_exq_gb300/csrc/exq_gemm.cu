@@ -294,8 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   StageMeta* meta = reinterpret_cast<StageMeta*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BT;
+  // token tiles vary fastest, so the CTAs that share a column tile's packed
+  // weights run together and the repeats come from L2
+  const int m0 = blockIdx.x * BT;
+  const int n0 = blockIdx.y * BN;
   const int kt0 = blockIdx.z * a.slabs_per;                      // this split's first slab
   const int n_iter = min(a.K / BK, kt0 + a.slabs_per) - kt0;     // >= 1 (host plan)
   const int tokens = min(BT, a.M - m0);                          // valid tokens of the tile
@@ -669,7 +671,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
   {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(w.N / BN, (M + BT - 1) / BT, plan.split);
+    cfg.gridDim = dim3((M + BT - 1) / BT, w.N / BN, plan.split);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

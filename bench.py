@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true",
                     help="time the prefill GEMM over the 70B shapes instead (one JSON line, TFLOPS per shape)")
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="time single GEMVs of the GPTQ 4096, GPTQ act-order 7B and EXL2 4.0 7B workloads "
+                         "instead (one JSON line, GB/s per shape and M)")
     return ap.parse_args()
 
 
@@ -252,6 +255,104 @@ def run_prefill(args, device):
         "config": {"workload": "prefill_70b_shapes", "value_is": "best shape"},
         "roofline": {"bound": "tensor", "peak": peak_bf16, "unit": "TFLOPS",
                      "peak_kind": "measured bf16 cuBLAS burst (fp16 runs at the same rate)"},
+        "shapes": shapes,
+    }
+
+
+def run_decode_sweep(args, device):
+    """Single exq_gemv calls of the decode workloads: GPTQ 4-bit g128 4096x4096
+    at M = 1 (no act-order); GPTQ act-order on the Llama-2-7B shapes at M in
+    {1, 4, 16}; EXL2 4.0 bpw (permuted) on the 7B shapes at M in {1, 8}.
+    Packed words are drawn uniformly on the device (the packing is a
+    bijection, so this is the distribution of uniform codes and zeros); each
+    timed call uses the next weight copy of a ring larger than twice L2, so
+    every call streams its weights from HBM. `--steps` calls (after
+    `--warmup`) captured in one CUDA graph and timed with CUDA events around a
+    replay; GB/s = packed bytes (codes + scales + zeros) per call / time."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    peak, peak_kind = measured_peaks()
+    ring_bytes = 300e6
+
+    def gptq(K, N, act, gen):
+        qw = torch.randint(0, 2 ** 32, (K // 8, N), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
+        qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
+                           generator=gen).to(torch.int32)
+        sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
+        perm = torch.randperm(K, device=device, generator=gen).int() if act else None
+        return exq.gptq_weight(qw, qz, sc, perm, K, N, 128, device=device)
+
+    def exl2(K, N, gen, rng):
+        bits = synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, rng)
+        off = np.zeros(bits.size + 1, np.int64)
+        off[1:] = np.cumsum(bits)
+        qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device,
+                           generator=gen).to(torch.int32)
+        sc = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
+        perm = torch.randperm(K, device=device, generator=gen).int()
+        return exq.exl2_weight(qw, off.astype(np.int32), sc, perm, K, N, device=device)
+
+    cases = [("gptq_g128 4096x4096", "gptq", 4096, 4096, False, (1,))]
+    for name, (K, N) in synth.LLAMA2_7B_SHAPES.items():
+        if name in ("q", "gate", "down"):
+            cases.append((f"gptq_act_order 7b {name} {K}x{N}", "gptq", K, N, True, (1, 4, 16)))
+    for name, (K, N) in synth.LLAMA2_7B_SHAPES.items():
+        if name in ("q", "gate", "down"):
+            cases.append((f"exl2_4.0bpw 7b {name} {K}x{N}", "exl2", K, N, True, (1, 8)))
+    shapes = {}
+    for label, fmt, K, N, act, Ms in cases:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(K * 7 + N)
+        rng = np.random.default_rng(K + N)
+        reps = max(2, int(ring_bytes // (K * N // 2)) + 1)
+        ring = [gptq(K, N, act, gen) if fmt == "gptq" else exl2(K, N, gen, rng) for _ in range(reps)]
+        for M in Ms:
+            x = torch.randn(M, K, device=device, generator=gen).half()
+            y = torch.empty(M, N, device=device, dtype=torch.float16)
+            ws = torch.zeros(exq.exq_gemv_workspace_size(ring[0], M), dtype=torch.uint8, device=device)
+            # one CUDA graph of `steps` calls (the host launch cost of a small
+            # call exceeds its GPU time; the graph times the GPU)
+            stream = torch.cuda.Stream(device=device)
+            stream.wait_stream(torch.cuda.current_stream(device))
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(args.warmup):
+                    exq.exq_gemv(ring[i % reps], x, y, workspace=ws)
+                torch.cuda.synchronize(device)
+                with torch.cuda.graph(graph, stream=stream):
+                    for i in range(args.steps):
+                        exq.exq_gemv(ring[i % reps], x, y, workspace=ws)
+            graph.replay()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize(device)
+            us = e0.elapsed_time(e1) * 1000 / args.steps
+            gbs = ring[0].packed_bytes / us / 1e3
+            shapes[f"{label} M={M}"] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        del ring
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the decode sweep")
+    return {
+        "metric": "decode GEMV weight GB/s (single calls)",
+        "value": max(v["GB/s"] for v in shapes.values()),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "decode_configs_gptq4096_gptq_act_order_7b_exl2_4p0_7b", "value_is": "best case",
+                   "l2": "weight ring larger than twice L2", "launch": "CUDA graph of the timed calls"},
+        "roofline": {"bound": "hbm", "peak": peak, "unit": UNIT, "peak_kind": peak_kind},
         "shapes": shapes,
     }
 
@@ -503,6 +604,10 @@ def main():
     if args.prefill:
         if rank == 0:
             print(json.dumps(run_prefill(args, torch.device("cuda", local))), flush=True)
+        return
+    if args.decode_sweep:
+        if rank == 0:
+            print(json.dumps(run_decode_sweep(args, torch.device("cuda", local))), flush=True)
         return
     if world > 1:
         import torch.distributed as dist

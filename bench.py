@@ -3,15 +3,19 @@
 
 Default workload: the full decode weight stream of a Llama-2-70B-shaped model
 at EXL2 4.0 bpw -- 80 layers x 7 quantized linears (q, k, v, o, gate, up,
-down), M = 1, fresh x ~ N(0,1) per linear, 560 exq_gemv calls back to back
-on one stream, captured once in a CUDA graph. One step = one token = all 560
-GEMVs; the weights (38.5 GB of packed codes + fp16 scales) are far larger
-than L2, so every step streams them from HBM.
+down), M = 1. As in the model, q, k and v read one activation vector and
+gate and up another, so each layer is four calls: exq_gemv_multi(q, k, v),
+exq_gemv(o), exq_gemv_multi(gate, up), exq_gemv(down), each with a fresh
+x ~ N(0,1); 320 calls back to back on one stream, captured once in a CUDA
+graph (``--ungrouped``: 560 exq_gemv calls, one per linear, each with its
+own x). One step = one token = all 560 matmuls; the weights (38.5 GB of
+packed codes + fp16 scales) are far larger than L2, so every step streams
+them from HBM.
 
 Prints one JSON line. ``value`` is the packed-weight throughput (qweight +
 scales bytes per step / time) with everything resident in HBM; ``e2e`` is the
-same metric when each step also copies its 560 activation vectors in from
-pinned host memory and its 560 outputs back; ``roofline`` relates the GEMV
+same metric when each step also copies its activation vectors (one per
+call) in from pinned host memory and its 560 outputs back; ``roofline`` relates the GEMV
 kernel to the measured HBM copy bandwidth; ``cpu_baseline`` is the CPU oracle
 on a bounded sample of the same workload.
 
@@ -43,6 +47,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = "decode_stream_70b"
 LINEARS = list(synth.LLAMA2_70B_SHAPES.items())
+# linears of a decoder layer that read the same activations
+GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
 GEMV_SOURCES = ["quantized_weight_exq_gb300/csrc/exq_gemv.cu", "quantized_weight_exq_gb300/csrc/exq_device.cuh"]
 
 
@@ -54,6 +60,9 @@ def parse_args():
     ap.add_argument("--impl", default="exq", choices=["exq", "reference"])
     ap.add_argument("--layers", type=int, default=80, help="decoder layers in the stream (80 = Llama-2-70B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ungrouped", action="store_true",
+                    help="decode stream as one exq_gemv per linear (each with its own x) instead of grouping "
+                         "the linears that share x (q/k/v, gate/up) into exq_gemv_multi calls")
     ap.add_argument("--prefill", action="store_true",
                     help="time the prefill GEMM over the 70B shapes instead (one JSON line, TFLOPS per shape)")
     ap.add_argument("--decode-sweep", action="store_true",
@@ -145,38 +154,62 @@ def bit_mix(layer: int, lin: int, K: int):
     return synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, synth.rng_for(0, wid, 7 * layer + lin, 4))
 
 
-def build_stream(exq, torch, layers: int, device):
-    """Device-resident packed weights for the whole stream. Packed codes are
-    uniform random words (a segment column's b words are a bijection of its
-    32 uniform b-bit codes); bits, scales and permutations follow the EXL2
-    4.0 bpw recipe."""
+def build_stream(exq, torch, layers: int, device, grouped: bool = True):
+    """Device-resident packed weights for the whole stream, as a list of
+    calls (weights, x, outputs). Packed codes are uniform random words (a
+    segment column's b words are a bijection of its 32 uniform b-bit codes);
+    bits, scales and permutations follow the EXL2 4.0 bpw recipe. Grouped:
+    one call (and one x) per group of linears that share activations."""
     wid = synth.WORKLOAD_IDS[WORKLOAD]
-    lin_list = []
-    x_total = sum(K for _, (K, N) in LINEARS) * layers
+    names = [n for n, _ in LINEARS]
+    groups = GROUPS if grouped else tuple((n,) for n in names)
+    x_total = sum(synth.LLAMA2_70B_SHAPES[grp[0]][0] for grp in groups) * layers
     y_total = sum(N for _, (K, N) in LINEARS) * layers
     x_all = torch.empty(x_total, dtype=torch.float16, device=device)
     y_all = torch.empty(y_total, dtype=torch.float16, device=device)
     xo = yo = 0
+    calls = []
     for layer in range(layers):
-        for i, (name, (K, N)) in enumerate(LINEARS):
-            gen = torch.Generator(device=device)
-            gen.manual_seed(int(synth.rng_for(0, wid, 7 * layer + i, 0).integers(0, 2 ** 62)))
-            bits = bit_mix(layer, i, K)
-            off = np.zeros(bits.size + 1, dtype=np.int64)
-            off[1:] = np.cumsum(bits.astype(np.int64))
-            rows = int(off[-1])
-            qweight = torch.randint(0, 2 ** 32, (rows, N), dtype=torch.int64, device=device,
-                                    generator=gen).to(torch.int32)
-            scales = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
-            perm = torch.randperm(K, device=device, generator=gen).to(torch.int32)
-            w = exq.exl2_weight(qweight, off.astype(np.int32), scales, perm, K, N, device=device)
-            x = x_all[xo:xo + K].view(1, K)
-            x.copy_(torch.randn(1, K, device=device, generator=gen).half())
-            y = y_all[yo:yo + N].view(1, N)
-            xo += K
-            yo += N
-            lin_list.append((w, x, y))
-    return lin_list, x_all, y_all
+        for grp in groups:
+            ws, ys = [], []
+            x = None
+            for name in grp:
+                i = names.index(name)
+                K, N = synth.LLAMA2_70B_SHAPES[name]
+                gen = torch.Generator(device=device)
+                gen.manual_seed(int(synth.rng_for(0, wid, 7 * layer + i, 0).integers(0, 2 ** 62)))
+                bits = bit_mix(layer, i, K)
+                off = np.zeros(bits.size + 1, dtype=np.int64)
+                off[1:] = np.cumsum(bits.astype(np.int64))
+                rows = int(off[-1])
+                qweight = torch.randint(0, 2 ** 32, (rows, N), dtype=torch.int64, device=device,
+                                        generator=gen).to(torch.int32)
+                scales = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
+                perm = torch.randperm(K, device=device, generator=gen).to(torch.int32)
+                ws.append(exq.exl2_weight(qweight, off.astype(np.int32), scales, perm, K, N, device=device))
+                if x is None:  # the group's activations: drawn with its first linear's generator
+                    x = x_all[xo:xo + K].view(1, K)
+                    x.copy_(torch.randn(1, K, device=device, generator=gen).half())
+                    xo += K
+                ys.append(y_all[yo:yo + N].view(1, N))
+                yo += N
+            calls.append((ws, x, ys))
+    return calls, x_all, y_all
+
+
+def issue_call(exq, call, workspace):
+    ws, x, ys = call
+    if len(ws) == 1:
+        exq.exq_gemv(ws[0], x, ys[0], workspace=workspace)
+    else:
+        exq.exq_gemv_multi(ws, x, ys, workspace=workspace)
+
+
+def call_workspace_size(exq, call) -> int:
+    ws, x, _ = call
+    if len(ws) == 1:
+        return exq.exq_gemv_workspace_size(ws[0], x.shape[0])
+    return exq.exq_gemv_multi_workspace_size(ws, x.shape[0])
 
 
 PREFILL_SHAPES = (("q", 8192, 8192), ("k", 8192, 1024), ("gate", 8192, 28672), ("down", 28672, 8192))
@@ -383,25 +416,27 @@ def run_exq(args, rank, world, device):
     import quantized_weight_exq_gb300 as exq
 
     torch.cuda.set_device(device)
-    lins, x_all, y_all = build_stream(exq, torch, args.layers, device)
-    bytes_per_step = sum(w.packed_bytes for w, _, _ in lins)
-    n_launch = len(lins)
-    # kernels per step: the GEMV, plus the act-order gather of x for a permuted layer
-    n_kernels = sum(2 if w.perm is not None else 1 for w, _, _ in lins)
+    grouped = not args.ungrouped
+    calls, x_all, y_all = build_stream(exq, torch, args.layers, device, grouped=grouped)
+    per_layer = len(calls) // args.layers
+    bytes_per_step = sum(w.packed_bytes for ws_, _, _ in calls for w in ws_)
+    n_linears = sum(len(ws_) for ws_, _, _ in calls)
+    n_launch = len(calls)
+    # kernels per step: the GEMV, plus one act-order gather of x for a call with a permuted layer
+    n_kernels = sum(2 if any(w.perm is not None for w in ws_) else 1 for ws_, _, _ in calls)
     # one zero-filled workspace for the whole stream, sized for its largest call
-    ws = torch.zeros(max(exq.exq_gemv_workspace_size(w, 1) for w, _, _ in lins[:len(LINEARS)]),
-                     dtype=torch.uint8, device=device)
+    ws = torch.zeros(max(call_workspace_size(exq, c) for c in calls[:per_layer]), dtype=torch.uint8, device=device)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(device=device)
     with torch.cuda.stream(stream):
-        for w, x, y in lins[:len(LINEARS)]:      # settle per-kernel attributes before capture
-            exq.exq_gemv(w, x, y, workspace=ws)
+        for c in calls[:per_layer]:      # settle per-kernel attributes before capture
+            issue_call(exq, c, ws)
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            for w, x, y in lins:
-                exq.exq_gemv(w, x, y, workspace=ws)
+            for c in calls:
+                issue_call(exq, c, ws)
     torch.cuda.synchronize()
     if exq.exq_get_last_device_error() != 0:
         raise RuntimeError("device error word set after warm-up")
@@ -482,7 +517,9 @@ def run_exq(args, rank, world, device):
             "M": 1,
             "bpw": 4.0,
             "bytes_per_step": bytes_per_step,
-            "gemv_per_step": n_launch,
+            "linears_per_step": n_linears,
+            "gemv_calls_per_step": n_launch,
+            "grouping": "q+k+v and gate+up share x: exq_gemv_multi" if grouped else "one exq_gemv per linear",
             "tokens_per_s": round(1000.0 / (t_ms / args.steps), 2),
             "pct_of_8TBps": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
             "l2": "inputs larger than L2 (the packed stream is 38.5 GB per step)",

@@ -158,6 +158,41 @@ size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M);
 exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Most layers one exq_gemv_multi call takes. */
+#define EXQ_GEMV_MAX_LAYERS 4
+
+/* Bytes of device workspace exq_gemv_multi needs for these n layers and M on
+ * the current device; 0 for an invalid group (see exq_gemv_multi) or M
+ * outside 1..16. exq_gemv_workspace_size(w, M) equals this with n = 1. */
+size_t exq_gemv_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M);
+
+/* exq_gemv_multi -- several decode matmuls that read the same activations,
+ * y_i = x . dequant(Wq_i) for i < n, in ONE launch: the q, k and v
+ * projections of an attention block, or the gate and up projections of an
+ * MLP. The architecture figure of the ExLlamaV2 blog post (section "The
+ * Solution", CUDA kernel layer) has the QKV projection as one kernel; here
+ * the layers stay separate tensors and only their work is pooled, so the SMs
+ * split the layers' combined weight stream evenly and the call pays one
+ * start-up and one tail instead of n.
+ *   w  host array of n descriptors (device pointers), 1 <= n <=
+ *      EXQ_GEMV_MAX_LAYERS, read during the call. All of one format, with
+ *      the same K and (GPTQ) the same group_size; N, the permutation (or
+ *      none) and every pointer may differ.
+ *   x  device fp16 [M, K], input-feature order, shared by every layer
+ *   y  host array of n device pointers, y[i] fp16 [M, w[i].N], fully
+ *      overwritten; the outputs must not overlap one another or x
+ *   workspace  as for exq_gemv, at least exq_gemv_multi_workspace_size()
+ *      bytes; the same zero-filled counters serve exq_gemv and
+ *      exq_gemv_multi calls in any order on one stream.
+ * Each y[i] is what exq_gemv gives for layer i up to the order of the fp32
+ * additions (the split over SMs differs), and the call is deterministic.
+ * The columns of all layers together may use at most 2048 tiles of 248
+ * columns (sum of N up to 507,904), else EXQ_ERR_UNSUPPORTED.
+ * Returns EXQ_ERR_INVALID_ARG for a bad n, a layer that fails the checks of
+ * exq_gemv, mixed formats, K or group sizes, or a bad output pointer. */
+exq_status exq_gemv_multi(const exq_weight* w, int32_t n, const uint16_t* x, int32_t M,
+                          uint16_t* const* y, void* workspace, size_t ws_bytes, void* stream);
+
 /* Bytes of device workspace exq_gemm needs for this layer and M (0 if none).
  * Two parts, both scratch: for a permuted layer, M * K * 2 bytes (rounded up
  * to 256) of activations gathered into stored-row order; and, when the grid

@@ -75,6 +75,18 @@ exq_status check_weight(const exq_weight* w) {
   return EXQ_OK;
 }
 
+// layers of one exq_gemv_multi call: each valid, one format, one K, one group size
+exq_status check_group(const exq_weight* w, int n) {
+  if (!w || n < 1 || n > EXQ_GEMV_MAX_LAYERS) return EXQ_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const exq_status st = check_weight(&w[i]);
+    if (st != EXQ_OK) return st;
+    if (w[i].format != w[0].format || w[i].K != w[0].K || w[i].group_size != w[0].group_size)
+      return EXQ_ERR_INVALID_ARG;
+  }
+  return EXQ_OK;
+}
+
 int current_cc() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -97,7 +109,7 @@ extern "C" exq_status exq_dequant(const exq_weight* w, uint16_t* W_out, void* st
 
 extern "C" size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M) {
   if (check_weight(w) != EXQ_OK || M < 1 || M > 16) return 0;
-  return gemv_workspace_bytes(*w, M);
+  return gemv_workspace_bytes(w, 1, M);
 }
 
 extern "C" exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
@@ -107,7 +119,24 @@ extern "C" exq_status exq_gemv(const exq_weight* w, const uint16_t* x, int32_t M
   if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
   if (M > 16) return EXQ_ERR_UNSUPPORTED;
   if (current_cc() < 100) return EXQ_ERR_CUDA;
-  return launch_gemv(*w, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+  return launch_gemv(w, 1, x, M, &y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exq_gemv_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M) {
+  if (check_group(w, n) != EXQ_OK || M < 1 || M > 16) return 0;
+  return gemv_workspace_bytes(w, n, M);
+}
+
+extern "C" exq_status exq_gemv_multi(const exq_weight* w, int32_t n, const uint16_t* x, int32_t M,
+                                     uint16_t* const* y, void* workspace, size_t ws_bytes, void* stream) {
+  const exq_status st = check_group(w, n);
+  if (st != EXQ_OK) return st;
+  if (!x || !y || !aligned16(x) || M < 1) return EXQ_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!y[i] || !aligned16(y[i])) return EXQ_ERR_INVALID_ARG;
+  if (M > 16) return EXQ_ERR_UNSUPPORTED;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_gemv(w, n, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M) {

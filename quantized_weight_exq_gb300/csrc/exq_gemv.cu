@@ -48,6 +48,7 @@
 //  * Every mbarrier wait is bounded; on expiry the kernel records a timeout
 //    in its device error word and the other roles stop at their next wait.
 #include <algorithm>
+#include <climits>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -87,30 +88,57 @@ static_assert(kTN % 8 == 0 && kTN / 8 <= 32, "a tile's zero words fit one warp")
 
 __host__ __device__ constexpr int slot_bytes_for(int M) { return ((kSlotX + M * kXRowBytes + 1023) / 1024) * 1024; }
 
+constexpr int kMaxLayers = EXQ_GEMV_MAX_LAYERS;  // layers of one launch (they share x and K)
+
 struct GemvMaps {
-  CUtensorMap w;  // qweight [n_word_rows, N] uint32, box 248 x 16
-  CUtensorMap s;  // scales [groups, N] fp16, box 248 x 4
-  CUtensorMap x;  // activations [M, K] fp16 (stored-row order), box 128 x M
+  CUtensorMap w[kMaxLayers];  // qweight [n_word_rows, N] uint32, box 248 x 32
+  CUtensorMap s[kMaxLayers];  // scales [groups, N] fp16, box 248 x 8
+  CUtensorMap x;              // activations [rows, K] fp16 (stored-row order), box 256 x M
+};
+
+// One layer of a launch. Its tiles are the global tiles tile0 .. (next
+// layer's tile0) - 1; unused entries have tile0 = INT_MAX.
+struct GemvLayer {
+  const uint32_t* seg_off;  // EXL2 [S + 1]
+  const uint32_t* qzeros;   // GPTQ [G, N / 8]
+  uint16_t* y;              // [M, N]
+  int N;
+  int n_word_rows;
+  int tile0;
+  int x_row;                // first row of the layer's activations in the x map
 };
 
 struct GemvArgs {
-  const uint32_t* seg_off;  // EXL2 [S + 1]
-  const uint32_t* qzeros;   // GPTQ [G, N / 8]
-  uint16_t* y;
+  GemvLayer L[kMaxLayers];
   uint32_t* counters;       // [n_tiles][8], zero between calls
   float* partials;          // [n_tiles][max_pieces][M][kTP]
-  int K, N, M;
+  int K, M;
   int S;                    // segments (K / 32)
   int gs_seg;               // GPTQ group size in segments
   int G;                    // GPTQ groups
-  int n_word_rows;
-  int n_tiles;
+  int n_tiles;              // tiles of all layers
   int total;                // units = n_tiles * S
   int max_pieces;
   int stages;
   int slot_bytes;
-  int off_bar;              // byte offset of the barriers, descriptors and table
+  int off_bar;              // byte offset of the barriers, descriptors and tables
 };
+
+// the layer that owns global tile T (constant indices into the parameters)
+__device__ __forceinline__ int layer_of(const GemvArgs& a, int T) {
+  int L = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxLayers; ++i) L += T >= a.L[i].tile0 ? 1 : 0;
+  return L;
+}
+
+__device__ __forceinline__ GemvLayer layer_params(const GemvArgs& a, int L) {
+  GemvLayer r = a.L[0];
+#pragma unroll
+  for (int i = 1; i < kMaxLayers; ++i)
+    if (L == i) r = a.L[i];
+  return r;
+}
 
 // Stage descriptor, written by the producer before the slot's copies.
 // The consumer K groups take the first h = (count + 1) / 2 segments and the rest.
@@ -119,7 +147,7 @@ struct GemvArgs {
 //      (EXL2) or its scale / zero row (GPTQ)
 //   b: EXL2: widths, 4 bits per segment (0 = skip the segment);
 //      GPTQ: position in its group of the first segment | of the second half's << 16
-//   c: tile
+//   c: tile (global over the launch's layers) | layer << 16
 //   d: first scale row of the slot (GPTQ group / EXL2 segment)
 struct Desc {
   uint32_t a, b, c, d;
@@ -314,24 +342,39 @@ __host__ __device__ __forceinline__ int share_owner(int u, int total, int G) {
   return static_cast<int>((static_cast<long long>(u + 1) * G - 1) / total);
 }
 
-// Act-order gather: xp[m][j] = x[m][perm[j]] (stored-row order), one element
-// per thread so that many loads are in flight. Out-of-range entries read as 0
-// and are reported. It also pulls the EXL2 segment table (seg_off, S + 1
-// entries, or NULL) into L2 for the GEMV that follows.
-__global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                                       int M, int K, uint16_t* __restrict__ xp,
-                                                       const uint32_t* __restrict__ seg_off, int S) {
+// Act-order gather for the layers of a launch: xp[l][m][j] = x[m][perm_l[j]]
+// (stored-row order; a layer without a permutation gets a plain copy), one
+// element per thread so that many loads are in flight, one grid row per
+// layer. Out-of-range entries read as 0 and are reported. It also pulls the
+// EXL2 segment tables (S + 1 entries each) into L2 for the GEMV that follows.
+struct GatherArgs {
+  const int32_t* perm[kMaxLayers];      // NULL: identity
+  const uint32_t* seg_off[kMaxLayers];  // NULL: nothing to prefetch
+};
+
+__global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restrict__ x,
+                                                       const __grid_constant__ GatherArgs ga, int M, int K,
+                                                       uint16_t* __restrict__ xp, int S) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  const int l = blockIdx.y;
+  const int32_t* perm = nullptr;
+  const uint32_t* seg_off = nullptr;
+#pragma unroll
+  for (int i = 0; i < kMaxLayers; ++i)
+    if (l == i) {
+      perm = ga.perm[i];
+      seg_off = ga.seg_off[i];
+    }
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;  // element of the layer's [M, K]
   if (seg_off && e * 32 <= S) asm volatile("prefetch.global.L2 [%0];" ::"l"(seg_off + e * 32));
   const bool in = e < M * K;
   const int j = in ? e % K : 0;
-  const int p = in ? __ldg(perm + j) : 0;  // the permutation is model state: read it before the wait
+  const int p = !in ? 0 : perm ? __ldg(perm + j) : j;  // the permutation is model state: read it before the wait
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!in) return;
   const bool ok = static_cast<unsigned>(p) < static_cast<unsigned>(K);
   if (!ok) atomicOr(&g_gemv_err, kDevErrBadPerm);
-  xp[e] = ok ? __ldg(x + static_cast<size_t>(e / K) * K + p) : static_cast<uint16_t>(0);
+  xp[static_cast<size_t>(l) * M * K + e] = ok ? __ldg(x + static_cast<size_t>(e / K) * K + p) : static_cast<uint16_t>(0);
 }
 
 __device__ __forceinline__ bool valid_width(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
@@ -351,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Desc* desc = reinterpret_cast<Desc*>(empty + kMaxStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(desc + kMaxStages);
   int* pend = const_cast<int*>(abort_flag) + 4;           // [kMaxStages] x copies held back (producer)
-  uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + a.off_bar + 512);  // EXL2 segment offsets [S + 1]
+  uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + a.off_bar + 512);  // EXL2 segment offsets [layers][S + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -370,46 +413,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // the layers this CTA's share touches
+    const int la = layer_of(a, u0 / a.S), lb = layer_of(a, (u1 - 1) / a.S);
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.s)) : "memory");
+#pragma unroll
+      for (int l = 0; l < kMaxLayers; ++l)
+        if (l >= la && l <= lb) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w[l])) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.s[l])) : "memory");
+        }
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
     }
     if constexpr (FMT == EXQ_FMT_EXL2) {
-      // the segment table is model state: copy it before the wait
-      for (int i = lane; i <= a.S; i += 32) cp_async4(smem_u32(tbl + i), a.seg_off + i);
+      // the segment tables are model state: copy them before the wait
+#pragma unroll
+      for (int l = 0; l < kMaxLayers; ++l)
+        if (l >= la && l <= lb)
+          for (int i = lane; i <= a.S; i += 32) cp_async4(smem_u32(tbl + l * (a.S + 1) + i), a.L[l].seg_off + i);
       asm volatile("cp.async.wait_all;" ::: "memory");
       __syncwarp();
     }
     const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXRowBytes;
     const uint32_t tx = kRowsPerStage * kTN * 4 + kScaleRows * kTN * 2 + x_bytes;
     int slot = 0, ephase = 0, issued = 0, npend = 0;
+    // the piece's layer: its index, tensor maps, first row of x, GPTQ zeros
+    const CUtensorMap* mw = &maps.w[0];
+    const CUtensorMap* ms = &maps.s[0];
+    int layer = 0, xrow = 0, nz = 0;
+    const uint32_t* qz = nullptr;
     bool waited = false, ok = true;
     auto release_x = [&]() {  // the activations may be read once the previous kernel is done
       asm volatile("griddepcontrol.wait;" ::: "memory");
       if (lane == 0)
         for (int i = 0; i < npend; ++i) {
-          const int sl = pend[i] & 0xFF, seg = pend[i] >> 8;
-          tma_load_2d(smem_u32(smem + sl * a.slot_bytes + kSlotX), &maps.x, seg * 32, 0, smem_u32(&full[sl]));
+          const int sl = pend[i] & 0xFF, seg = (pend[i] >> 8) & 0xFFFF, xr = static_cast<int>(pend[i] >> 24);
+          tma_load_2d(smem_u32(smem + sl * a.slot_bytes + kSlotX), &maps.x, seg * 32, xr, smem_u32(&full[sl]));
         }
       npend = 0;
       waited = true;
     };
     // one stage into the next slot; false once a wait gave up
-    auto issue = [&](uint32_t da, uint32_t widths, int tile, int row0, int srow, bool bad) -> bool {
+    // tile: global (for the consumers), lt: in the layer (for the copies)
+    auto issue = [&](uint32_t da, uint32_t widths, int tile, int lt, int row0, int srow, bool bad) -> bool {
       if (!waited && issued >= a.stages) release_x();  // the ring is about to wrap
       if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag)) return false;
       uint8_t* st = smem + slot * a.slot_bytes;
       const uint32_t fb = smem_u32(&full[slot]);
-      if (lane == 0) desc[slot] = Desc{da, widths, static_cast<uint32_t>(tile), static_cast<uint32_t>(srow)};
+      if (lane == 0)
+        desc[slot] = Desc{da, widths, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16),
+                          static_cast<uint32_t>(srow)};
       if constexpr (FMT == EXQ_FMT_GPTQ4) {
         if (!bad) {
-          const int nz = a.N / 8, cw = tile * (kTN / 8) + lane;
+          const int cw = lt * (kTN / 8) + lane;
 #pragma unroll
           for (int r = 0; r < kScaleRows; ++r)
             if (srow + r < a.G && cw < nz && lane < kTN / 8)
               cp_async4(smem_u32(st + kSlotZ + r * kZeroRowBytes + lane * 4),
-                        a.qzeros + static_cast<size_t>(srow + r) * nz + cw);
+                        qz + static_cast<size_t>(srow + r) * nz + cw);
           cp_async_arrive(fb);  // one more pending arrival, made when this lane's copies land
         }
       }
@@ -419,12 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(fb);
         } else {
           mbar_expect_tx(fb, tx);
-          tma_load_2d(smem_u32(st + kSlotW), &maps.w, tile * kTN, row0, fb);
-          tma_load_2d(smem_u32(st + kSlotS), &maps.s, tile * kTN, srow, fb);
-          if (waited) tma_load_2d(smem_u32(st + kSlotX), &maps.x, static_cast<int>(da & 0xFFFFu) * 32, 0, fb);
+          tma_load_2d(smem_u32(st + kSlotW), mw, lt * kTN, row0, fb);
+          tma_load_2d(smem_u32(st + kSlotS), ms, lt * kTN, srow, fb);
+          if (waited) tma_load_2d(smem_u32(st + kSlotX), &maps.x, static_cast<int>(da & 0xFFFFu) * 32, xrow, fb);
         }
       }
-      if (!bad && !waited) pend[npend++] = slot | (static_cast<int>(da & 0xFFFFu) << 8);
+      if (!bad && !waited) pend[npend++] = slot | (static_cast<int>(da & 0xFFFFu) << 8) | (xrow << 24);
       ++issued;
       if (++slot == a.stages) {
         slot = 0;
@@ -435,6 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int u = u0; u < u1 && ok;) {
       const int tile = u / a.S;
+      layer = layer_of(a, tile);
+      const GemvLayer ly = layer_params(a, layer);
+      const int lt = tile - ly.tile0;
+      mw = &maps.w[layer];
+      ms = &maps.s[layer];
+      xrow = ly.x_row;
+      qz = ly.qzeros;
+      nz = ly.N / 8;
       const int sa = u - tile * a.S;
       const int sb = min(a.S, sa + (u1 - u));
       u += sb - sa;
@@ -453,9 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // segments from seg (at most four) whose widths add up to at most 16
           const int sk = seg + lane;
           const bool cand = lane < kSegsPerStage && sk < sb;
-          const uint32_t e0 = cand ? tbl[sk] : 0u, e1 = cand ? tbl[sk + 1] : 0u;
+          const uint32_t* ltbl = tbl + layer * (a.S + 1);
+          const uint32_t e0 = cand ? ltbl[sk] : 0u, e1 = cand ? ltbl[sk + 1] : 0u;
           const int b = static_cast<int>(e1) - static_cast<int>(e0);
-          const bool good = cand && valid_width(b) && e1 <= static_cast<uint32_t>(a.n_word_rows);
+          const bool good = cand && valid_width(b) && e1 <= static_cast<uint32_t>(ly.n_word_rows);
           int ps = good ? b : 0;  // inclusive prefix sum of the widths over lanes 0..7
 #pragma unroll
           for (int d = 1; d < 8; d <<= 1) {
@@ -487,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t da = static_cast<uint32_t>(seg) | (static_cast<uint32_t>(n) << 16) | (first ? kDescFirst : 0u) |
                             (last ? kDescLast : 0u) | (half << 24);
-        ok = issue(da, db, tile, row0, srow, bad);
+        ok = issue(da, db, tile, lt, row0, srow, bad);
         seg += n;
         first = false;
       }
@@ -525,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
     const uint8_t* sl = smem + slot * a.slot_bytes;
-    const int seg0 = static_cast<int>(d.a & 0xFFFFu), n = static_cast<int>((d.a >> 16) & 15u);
+    const int n = static_cast<int>((d.a >> 16) & 15u);
     if (d.a & kDescFirst) zero4<MT>(acc);
     const uint8_t* wrow = sl + kSlotW + 128 * w + 16 * g;
     const uint8_t* xrow0 = sl + kSlotX + tok[0] * kXRowBytes + 16 * t;
@@ -595,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- this warp's share of the piece: 32 columns, one K group. Every
       // (piece, K group) leaves fp32 partial sums; the last of the tile's
       // 2P arrivals at the column group's counter adds them in order.
-      const int tile = static_cast<int>(d.c);
+      const int tile = static_cast<int>(d.c & 0xFFFFu);
       const int first = share_owner(tile * a.S, a.total, G);
       const int P2 = 2 * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
       const int pslot = 2 * (static_cast<int>(blockIdx.x) - first) + kg;
@@ -624,9 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       last = __shfl_sync(0xffffffffu, last, 0);
       __syncwarp();
       if (last) {
+        const GemvLayer* lp = &a.L[0] + (d.c >> 16);
         const float* base = a.partials + static_cast<size_t>(tile) * a.max_pieces * a.M * kTP + 32 * w + lane;
-        const int n = tile * kTN + 32 * w + lane;
-        const bool n_ok = 32 * w + lane < kTN && n < a.N;
+        const int n = (tile - lp->tile0) * kTN + 32 * w + lane;
+        const bool n_ok = 32 * w + lane < kTN && n < lp->N;
         const size_t stride = static_cast<size_t>(a.M) * kTP;
         for (int m = 0; m < a.M; ++m) {
           // pieces added in piece order, 32 loads in flight at a time
@@ -639,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v += q[i];
           }
-          if (n_ok) a.y[static_cast<size_t>(m) * a.N + n] = __half_as_ushort(__float2half_rn(v));
+          if (n_ok) lp->y[static_cast<size_t>(m) * lp->N + n] = __half_as_ushort(__float2half_rn(v));
         }
       }
     }
@@ -673,18 +743,27 @@ constexpr int kSmemPerCta = 210 * 1024;  // one CTA per SM
 
 struct Plan {
   int G, S, n_tiles, total, max_pieces, stages, slot_bytes, off_bar;
-  size_t smem;         // dynamic shared memory bytes (with the alignment slack)
-  size_t ws_partials;  // bytes of the partial sums
-  size_t ws_bytes;     // counters + partials (+ M * K * 2 for a permuted layer's gathered x)
+  int tile0[kMaxLayers + 1];  // first global tile of each layer; tile0[n] = n_tiles
+  bool gather;                // some layer has a permutation: x is gathered per layer
+  size_t smem;                // dynamic shared memory bytes (with the alignment slack)
+  size_t ws_partials;         // bytes of the partial sums
+  size_t ws_bytes;            // counters + partials (+ n * M * K * 2 of gathered x)
 };
 
-// Layout of one launch on a device with `sm_count` SMs; false if this
-// kernel cannot take the layer.
-bool make_plan(const exq_weight& w, int M, int sm_count, Plan& p) {
-  if (M < 1 || M > 16) return false;
-  p.S = w.K / 32;
+// Layout of one launch over n layers that share K on a device with
+// `sm_count` SMs; false if this kernel cannot take them.
+bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
+  if (M < 1 || M > 16 || n < 1 || n > kMaxLayers) return false;
+  p.S = w[0].K / 32;
   if (p.S > 0xFFFF) return false;  // segment indices travel in 16 bits
-  p.n_tiles = (w.N + kTN - 1) / kTN;
+  p.n_tiles = 0;
+  p.gather = false;
+  for (int i = 0; i < n; ++i) {
+    p.tile0[i] = p.n_tiles;
+    p.n_tiles += (w[i].N + kTN - 1) / kTN;
+    p.gather = p.gather || w[i].perm != nullptr;
+  }
+  p.tile0[n] = p.n_tiles;
   if (p.n_tiles * kColGroups * 4 > kCounterBytes) return false;
   const long long total = static_cast<long long>(p.n_tiles) * p.S;
   if (total >= (1ll << 31)) return false;
@@ -696,8 +775,8 @@ bool make_plan(const exq_weight& w, int M, int sm_count, Plan& p) {
   }
   p.G = std::max(1, std::min(G, p.total));
   p.slot_bytes = slot_bytes_for(M);
-  const size_t table = w.format == EXQ_FMT_EXL2 ? align_up(static_cast<size_t>(p.S + 1) * 4, 16) : 0;
-  const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment table, alignment slack
+  const size_t table = w[0].format == EXQ_FMT_EXL2 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
+  const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment tables, alignment slack
   const long long room = static_cast<long long>(kSmemPerCta) - static_cast<long long>(fixed);
   p.stages = static_cast<int>(std::min<long long>(kMaxStages, room / p.slot_bytes));
   if (p.stages < 2) return false;
@@ -708,7 +787,8 @@ bool make_plan(const exq_weight& w, int M, int sm_count, Plan& p) {
   const int min_share = std::max(1, p.total / p.G);
   p.max_pieces = 2 * std::min(p.G, (p.S - 1) / min_share + 2);
   p.ws_partials = align_up(static_cast<size_t>(p.n_tiles) * p.max_pieces * M * kTP * 4, 256);
-  p.ws_bytes = kCounterBytes + p.ws_partials + (w.perm ? align_up(static_cast<size_t>(M) * w.K * 2, 256) : 0);
+  p.ws_bytes = kCounterBytes + p.ws_partials +
+               (p.gather ? align_up(static_cast<size_t>(n) * M * w[0].K * 2, 256) : 0);
   return true;
 }
 
@@ -717,15 +797,15 @@ bool g_attr_done[64][4];
 
 }  // namespace
 
-size_t gemv_workspace_bytes(const exq_weight& w, int M) {
+size_t gemv_workspace_bytes(const exq_weight* w, int n, int M) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   Plan plan{};
-  if (!make_plan(w, M, device_info(dev).sm_count, plan)) return 0;
+  if (!make_plan(w, n, M, device_info(dev).sm_count, plan)) return 0;
   return plan.ws_bytes;
 }
 
-exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
+exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
@@ -733,14 +813,15 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   if (di.sm_count <= 0 || dev >= 64) return EXQ_ERR_CUDA;
 
   Plan plan{};
-  if (!make_plan(w, M, di.sm_count, plan)) return EXQ_ERR_UNSUPPORTED;
+  if (!make_plan(w, n, M, di.sm_count, plan)) return EXQ_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < plan.ws_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return EXQ_ERR_INVALID_ARG;
+  const exq_weight& w0 = w[0];
 
-  KernelFn fn = pick_kernel(w.format, M);
+  KernelFn fn = pick_kernel(w0.format, M);
   {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    bool& done = g_attr_done[dev][variant_index(w.format, M)];
+    bool& done = g_attr_done[dev][variant_index(w0.format, M)];
     if (!done) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess)
         return EXQ_ERR_CUDA;
@@ -758,19 +839,23 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // act-order: gather x into stored-row order once, into the workspace
+  // act-order: gather x into each layer's stored-row order once, into the workspace
   const uint16_t* xs_src = x;
-  if (w.perm) {
+  if (plan.gather) {
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws + kCounterBytes + plan.ws_partials);
-    const int threads = M * w.K;
+    GatherArgs ga{};
+    for (int i = 0; i < n; ++i) {
+      ga.perm[i] = w[i].perm;
+      ga.seg_off[i] = w[i].seg_word_off;
+    }
+    const int threads = M * w0.K;  // per layer
     cudaLaunchConfig_t gcfg{};
-    gcfg.gridDim = dim3((threads + 255) / 256, 1, 1);
+    gcfg.gridDim = dim3((threads + 255) / 256, n, 1);
     gcfg.blockDim = dim3(256, 1, 1);
     gcfg.stream = stream;
     gcfg.attrs = attrs;
     gcfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&gcfg, gather_x_kernel, x, w.perm, M, w.K, xp, w.seg_word_off, w.K / 32) !=
-        cudaSuccess) {
+    if (cudaLaunchKernelEx(&gcfg, gather_x_kernel, x, ga, M, w0.K, xp, w0.K / 32) != cudaSuccess) {
       cudaGetLastError();
       return EXQ_ERR_CUDA;
     }
@@ -779,28 +864,38 @@ exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
 
   GemvMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  const int scale_rows = w.format == EXQ_FMT_GPTQ4 ? w.n_groups : w.K / 32;
-  if (!encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.qweight, w.N, w.n_word_rows,
-                 static_cast<uint64_t>(w.N) * 4, kTN, kRowsPerStage) ||
-      !encode_2d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, w.scales, w.N, scale_rows, static_cast<uint64_t>(w.N) * 2,
-                 kTN, kScaleRows) ||
-      !encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xs_src, w.K, M, static_cast<uint64_t>(w.K) * 2,
-                 kSegsPerStage * 32, M))
+  GemvArgs args{};
+  const int scale_rows = w0.format == EXQ_FMT_GPTQ4 ? w0.n_groups : w0.K / 32;
+  for (int i = 0; i < kMaxLayers; ++i) {
+    GemvLayer& l = args.L[i];
+    if (i >= n) {
+      l.tile0 = INT_MAX;
+      continue;
+    }
+    if (!encode_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[i].qweight, w[i].N, w[i].n_word_rows,
+                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage) ||
+        !encode_2d(&maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, w[i].scales, w[i].N, scale_rows,
+                   static_cast<uint64_t>(w[i].N) * 2, kTN, kScaleRows))
+      return EXQ_ERR_CUDA;
+    l.seg_off = w[i].seg_word_off;
+    l.qzeros = w[i].qzeros;
+    l.y = y[i];
+    l.N = w[i].N;
+    l.n_word_rows = w[i].n_word_rows;
+    l.tile0 = plan.tile0[i];
+    l.x_row = plan.gather ? i * M : 0;
+  }
+  if (!encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xs_src, w0.K, static_cast<uint64_t>(plan.gather ? n : 1) * M,
+                 static_cast<uint64_t>(w0.K) * 2, kSegsPerStage * 32, M))
     return EXQ_ERR_CUDA;
 
-  GemvArgs args{};
-  args.seg_off = w.seg_word_off;
-  args.qzeros = w.qzeros;
-  args.y = y;
   args.counters = reinterpret_cast<uint32_t*>(ws);
   args.partials = reinterpret_cast<float*>(ws + kCounterBytes);
-  args.K = w.K;
-  args.N = w.N;
+  args.K = w0.K;
   args.M = M;
   args.S = plan.S;
-  args.gs_seg = w.format == EXQ_FMT_GPTQ4 ? w.group_size / 32 : 1;
-  args.G = w.format == EXQ_FMT_GPTQ4 ? w.n_groups : plan.S;
-  args.n_word_rows = w.n_word_rows;
+  args.gs_seg = w0.format == EXQ_FMT_GPTQ4 ? w0.group_size / 32 : 1;
+  args.G = w0.format == EXQ_FMT_GPTQ4 ? w0.n_groups : plan.S;
   args.n_tiles = plan.n_tiles;
   args.total = plan.total;
   args.max_pieces = plan.max_pieces;

@@ -37,9 +37,10 @@ EncodeTiled tensor_map_encoder();
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
                uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
-exq_status launch_gemv(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
+// n layers (1..EXQ_GEMV_MAX_LAYERS) of one format and K that share x
+exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);
-size_t gemv_workspace_bytes(const exq_weight& w, int M);
+size_t gemv_workspace_bytes(const exq_weight* w, int n, int M);
 exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t stream);
 exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);

@@ -29,9 +29,12 @@ EXQ_FMT_EXL2 = 2
 # every symbol include/exq.h declares
 EXPORTED = (
     "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
-    "exq_gemv", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
+    "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error",
 )
+
+# most layers one exq_gemv_multi call takes (EXQ_GEMV_MAX_LAYERS)
+GEMV_MAX_LAYERS = 4
 
 # size of the static scratch array exq_gemm_noalloc uses (EXQ_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -66,6 +69,8 @@ def _load():
         "exq_dequant": (st, [W, P, P]),
         "exq_gemv_workspace_size": (sz, [W, i32]),
         "exq_gemv": (st, [W, P, i32, P, P, sz, P]),
+        "exq_gemv_multi_workspace_size": (sz, [W, i32, i32]),
+        "exq_gemv_multi": (st, [W, i32, P, i32, P, P, sz, P]),
         "exq_gemm_workspace_size": (sz, [W, i32]),
         "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
         "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
@@ -225,8 +230,11 @@ def gemv_workspace(w: Weight, M: int):
     across calls. exq_gemv leaves it zeroed, so calls ordered on one stream can
     share it; calls that may overlap on the GPU need their own (torch.zeros of
     exq_gemv_workspace_size bytes)."""
+    return _shared_workspace(exq_gemv_workspace_size(w, M))
+
+
+def _shared_workspace(need: int):
     import torch
-    need = exq_gemv_workspace_size(w, M)
     dev = torch.cuda.current_device()
     buf = _gemv_ws.get(dev)
     if buf is None or buf.numel() < need:
@@ -242,6 +250,28 @@ def exq_gemv(w: Weight, x, y, workspace=None, stream=None):
     _check(_lib.exq_gemv(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), workspace.data_ptr(),
                          ws_bytes, _stream_ptr(stream)), "exq_gemv")
     return y
+
+
+def _desc_array(ws):
+    return (exq_weight * len(ws))(*[w.desc() for w in ws])
+
+
+def exq_gemv_multi_workspace_size(ws, M: int) -> int:
+    return int(_lib.exq_gemv_multi_workspace_size(_desc_array(ws), len(ws), M))
+
+
+def exq_gemv_multi(ws, x, ys, workspace=None, stream=None):
+    """y_i = x . dequant(ws[i]) for the layers ws (one format, one K), in one
+    launch. ``ys`` are the outputs, one per layer."""
+    if len(ws) != len(ys):
+        raise ExqError(EXQ_ERR_INVALID_ARG, "exq_gemv_multi")
+    if workspace is None:
+        workspace = _shared_workspace(exq_gemv_multi_workspace_size(ws, x.shape[0]))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    yp = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
+    _check(_lib.exq_gemv_multi(_desc_array(ws), len(ws), x.data_ptr(), x.shape[0], yp, workspace.data_ptr(),
+                               ws_bytes, _stream_ptr(stream)), "exq_gemv_multi")
+    return ys
 
 
 def exq_gemm_workspace_size(w: Weight, M: int) -> int:

@@ -116,3 +116,37 @@ def test_device_entry_points_validate_on_host(exq):
     dp = _desc(exq, perm=0x70000)
     assert lib.exq_gemm_workspace_size(ctypes.byref(dp), 128) == 128 * 256 * 2
     assert lib.exq_gemm(ctypes.byref(dp), 0x50000, 128, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+
+
+def test_gemv_multi_validates_on_host(exq):
+    from quantized_weight_exq_gb300 import exq as mod
+    lib = mod._lib
+
+    def call(descs, M=1, ys=None, x=0x50000):
+        arr = (exq.exq_weight * max(len(descs), 1))(*descs)
+        ys = [0x60000 + 0x1000 * i for i in range(len(descs))] if ys is None else ys
+        yp = (ctypes.c_void_p * max(len(ys), 1))(*ys)
+        return lib.exq_gemv_multi(arr, len(descs), x, M, yp, None, 0, None)
+
+    d = _desc(exq)
+    assert call([]) == exq.EXQ_ERR_INVALID_ARG                                    # no layers
+    assert call([d] * 5) == exq.EXQ_ERR_INVALID_ARG                               # more than EXQ_GEMV_MAX_LAYERS
+    assert call([d, _desc(exq, K=512, n_groups=4, n_word_rows=64)]) == exq.EXQ_ERR_INVALID_ARG  # mixed K
+    assert call([d, _desc(exq, group_size=64, n_groups=4)]) == exq.EXQ_ERR_INVALID_ARG          # mixed group size
+    exl2 = _desc(exq, format=2, group_size=32, n_groups=8, n_word_rows=32, qzeros=None, seg_word_off=0x40000)
+    assert call([d, exl2]) == exq.EXQ_ERR_INVALID_ARG                             # mixed formats
+    assert call([d, _desc(exq, N=60)]) == exq.EXQ_ERR_INVALID_ARG                 # a bad layer
+    assert call([d, d], ys=[0x60000, None]) == exq.EXQ_ERR_INVALID_ARG           # a missing output
+    assert call([d, d], ys=[0x60000, 0x61008]) == exq.EXQ_ERR_INVALID_ARG        # a misaligned output
+    assert call([d, d], x=0x50008) == exq.EXQ_ERR_INVALID_ARG
+    assert call([d, d], M=0) == exq.EXQ_ERR_INVALID_ARG
+    assert call([d, d], M=17) == exq.EXQ_ERR_UNSUPPORTED
+    assert lib.exq_gemv_multi(None, 1, 0x50000, 1, None, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+    arr = (exq.exq_weight * 2)(d, d)
+    assert lib.exq_gemv_multi(arr, 2, 0x50000, 1, None, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+    # the workspace size is 0 for an invalid group or M
+    assert lib.exq_gemv_multi_workspace_size(arr, 5, 1) == 0
+    assert lib.exq_gemv_multi_workspace_size(arr, 0, 1) == 0
+    assert lib.exq_gemv_multi_workspace_size(arr, 2, 17) == 0
+    mixed = (exq.exq_weight * 2)(d, exl2)
+    assert lib.exq_gemv_multi_workspace_size(mixed, 2, 1) == 0

@@ -295,7 +295,9 @@ def run_prefill(args, device):
 def run_decode_sweep(args, device):
     """Single exq_gemv calls of the decode workloads: GPTQ 4-bit g128 4096x4096
     at M = 1 (no act-order); GPTQ act-order on the Llama-2-7B shapes at M in
-    {1, 4, 16}; EXL2 4.0 bpw (permuted) on the 7B shapes at M in {1, 8}.
+    {1, 4, 16}; EXL2 4.0 bpw (permuted) on the 7B shapes at M in {1, 8}. Then
+    the 7B linears that share x (q+k+v, gate+up) as one exq_gemv_multi call
+    each, in both formats.
     Packed words are drawn uniformly on the device (the packing is a
     bijection, so this is the distribution of uniform codes and zeros); each
     timed call uses the next weight copy of a ring larger than twice L2, so
@@ -330,24 +332,37 @@ def run_decode_sweep(args, device):
         perm = torch.randperm(K, device=device, generator=gen).int()
         return exq.exl2_weight(qw, off.astype(np.int32), sc, perm, K, N, device=device)
 
-    cases = [("gptq_g128 4096x4096", "gptq", 4096, 4096, False, (1,))]
+    cases = [("gptq_g128 4096x4096", "gptq", 4096, (4096,), False, (1,))]
     for name, (K, N) in synth.LLAMA2_7B_SHAPES.items():
         if name in ("q", "gate", "down"):
-            cases.append((f"gptq_act_order 7b {name} {K}x{N}", "gptq", K, N, True, (1, 4, 16)))
+            cases.append((f"gptq_act_order 7b {name} {K}x{N}", "gptq", K, (N,), True, (1, 4, 16)))
     for name, (K, N) in synth.LLAMA2_7B_SHAPES.items():
         if name in ("q", "gate", "down"):
-            cases.append((f"exl2_4.0bpw 7b {name} {K}x{N}", "exl2", K, N, True, (1, 8)))
+            cases.append((f"exl2_4.0bpw 7b {name} {K}x{N}", "exl2", K, (N,), True, (1, 8)))
+    for grp in (("q", "k", "v"), ("gate", "up")):
+        K = synth.LLAMA2_7B_SHAPES[grp[0]][0]
+        Ns = tuple(synth.LLAMA2_7B_SHAPES[n][1] for n in grp)
+        tag = "+".join(grp)
+        cases.append((f"gptq_act_order 7b {tag} grouped", "gptq", K, Ns, True, (1, 4, 16)))
+        cases.append((f"exl2_4.0bpw 7b {tag} grouped", "exl2", K, Ns, True, (1, 8)))
     shapes = {}
-    for label, fmt, K, N, act, Ms in cases:
+    for label, fmt, K, Ns, act, Ms in cases:
         gen = torch.Generator(device=device)
-        gen.manual_seed(K * 7 + N)
-        rng = np.random.default_rng(K + N)
-        reps = max(2, int(ring_bytes // (K * N // 2)) + 1)
-        ring = [gptq(K, N, act, gen) if fmt == "gptq" else exl2(K, N, gen, rng) for _ in range(reps)]
+        gen.manual_seed(K * 7 + sum(Ns) + len(Ns) - 1)
+        rng = np.random.default_rng(K + sum(Ns) + len(Ns) - 1)
+        reps = max(2, int(ring_bytes // (K * sum(Ns) // 2)) + 1)
+        ring = [[gptq(K, N, act, gen) if fmt == "gptq" else exl2(K, N, gen, rng) for N in Ns] for _ in range(reps)]
+
+        def call(i, x, ys, ws):
+            if len(Ns) == 1:
+                exq.exq_gemv(ring[i % reps][0], x, ys[0], workspace=ws)
+            else:
+                exq.exq_gemv_multi(ring[i % reps], x, ys, workspace=ws)
+
         for M in Ms:
             x = torch.randn(M, K, device=device, generator=gen).half()
-            y = torch.empty(M, N, device=device, dtype=torch.float16)
-            ws = torch.zeros(exq.exq_gemv_workspace_size(ring[0], M), dtype=torch.uint8, device=device)
+            ys = [torch.empty(M, N, device=device, dtype=torch.float16) for N in Ns]
+            ws = torch.zeros(exq.exq_gemv_multi_workspace_size(ring[0], M), dtype=torch.uint8, device=device)
             # one CUDA graph of `steps` calls (the host launch cost of a small
             # call exceeds its GPU time; the graph times the GPU)
             stream = torch.cuda.Stream(device=device)
@@ -355,11 +370,11 @@ def run_decode_sweep(args, device):
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.stream(stream):
                 for i in range(args.warmup):
-                    exq.exq_gemv(ring[i % reps], x, y, workspace=ws)
+                    call(i, x, ys, ws)
                 torch.cuda.synchronize(device)
                 with torch.cuda.graph(graph, stream=stream):
                     for i in range(args.steps):
-                        exq.exq_gemv(ring[i % reps], x, y, workspace=ws)
+                        call(i, x, ys, ws)
             graph.replay()
             torch.cuda.synchronize(device)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -368,7 +383,7 @@ def run_decode_sweep(args, device):
             e1.record()
             torch.cuda.synchronize(device)
             us = e0.elapsed_time(e1) * 1000 / args.steps
-            gbs = ring[0].packed_bytes / us / 1e3
+            gbs = sum(w.packed_bytes for w in ring[0]) / us / 1e3
             shapes[f"{label} M={M}"] = {"us": round(us, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
         del ring
     if exq.exq_get_last_device_error() != 0:

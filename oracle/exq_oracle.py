@@ -39,8 +39,15 @@ Readings where the pages are silent (each one is listed in the design doc):
 * GPTQ zero points are stored as the zero itself (no +1 offset), 4 bits,
   packed 8 per uint32 along N. EXL2 is symmetric: zero = 2^(b-1).
 * GPTQ scales are fp16 [G, N]; EXL2 scales are fp16 [S, N], one per
-  (segment, column). (The pages' two-level 4-bit scale x per-column max scale
-  is a later format variant and is not modelled here.)
+  (segment, column).
+* EXL2 with two-level scales (the q_scale / q_scale_max pair of "Step 3:
+  Quantization Application", multiplied together in "How the Fused CUDA
+  Kernel Works"): a 4-bit code c per (segment, column), packed 8 per uint32
+  along N (nibble i of word k = column 8k + i), and one fp16 maximum m per
+  column. The pages do not say how a code maps to a fraction; the reading
+  here is (c + 1) / 16, so c = 15 is the maximum. The segment's fp16 scale is
+  s = fp16_RNE(((c + 1) / 16) * m) (one rounding: the product is exact), and
+  the weight is then w = fp16_RNE((q - z) * s) as for fp16 scales.
 * Dequantised weight w = fp16_RNE((q - z) * s): the product is exact in
   float32 and float64 (at most 8 + 11 significant bits), so there is exactly
   one rounding.
@@ -59,7 +66,8 @@ __all__ = [
     "gptq_perm_from_g_idx", "pack_gptq", "unpack_gptq_codes", "unpack_gptq_zeros",
     "dequant_gptq", "dequant_gptq_definitional",
     "exl2_seg_word_off", "pack_exl2", "unpack_exl2_codes", "dequant_exl2",
-    "dequant_exl2_definitional", "matmul", "quantize_rtn", "EXL2_BITS", "SEGMENT_ROWS",
+    "dequant_exl2_definitional", "pack_exl2_qscale", "unpack_exl2_qscale", "exl2_two_level_scales",
+    "dequant_exl2_qscale", "matmul", "quantize_rtn", "EXL2_BITS", "SEGMENT_ROWS",
 ]
 
 # ----------------------------------------------------------------------------
@@ -343,6 +351,59 @@ def dequant_exl2_definitional(q_st, bits, s, perm) -> np.ndarray:
     z = (1 << (bits[seg] - 1)).astype(np.int64)
     w = (q_st.astype(np.int64) - z[:, None]).astype(np.float64) * _as_f64(s)[seg]
     return _scatter_rows(fp16_bits_from_float64(w), perm)
+
+
+# ----------------------------------------------------------------------------
+# EXL2 with two-level scales (4-bit group scale code x per-column maximum)
+# ----------------------------------------------------------------------------
+
+def pack_exl2_qscale(codes) -> np.ndarray:
+    """uint8 [S, N] codes 0..15 -> uint32 [S, N/8], one bit at a time:
+    bit t of column n = 8k + i goes to bit 4i + t of word k."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    S, N = codes.shape
+    if N % 8 or (codes > 15).any():
+        raise ValueError("N must be a multiple of 8 and codes below 16")
+    out = np.zeros((S, N // 8), dtype=np.uint32)
+    for n in range(N):
+        k, i = divmod(n, 8)
+        for t in range(4):
+            bit = ((codes[:, n] >> t) & 1).astype(np.uint32)
+            out[:, k] |= bit << np.uint32(4 * i + t)
+    return out
+
+
+def unpack_exl2_qscale(words, N: int) -> np.ndarray:
+    """uint32 [S, N/8] -> uint8 [S, N] codes, one bit at a time."""
+    words = np.asarray(words, dtype=np.uint32)
+    out = np.zeros((words.shape[0], N), dtype=np.uint8)
+    for n in range(N):
+        k, i = divmod(n, 8)
+        for t in range(4):
+            bit = ((words[:, k] >> np.uint32(4 * i + t)) & np.uint32(1)).astype(np.uint8)
+            out[:, n] |= bit << t
+    return out
+
+
+def exl2_two_level_scales(codes, scale_max) -> np.ndarray:
+    """fp16 bits [S, N] of s(g, n) = fp16_RNE(((c(g, n) + 1) / 16) * m(n)).
+
+    codes uint8 [S, N] (0..15), scale_max fp16 [N]. The float64 product is
+    exact, so this is the single rounding of the definition."""
+    c = np.asarray(codes, dtype=np.int64)
+    m = _as_f64(scale_max)
+    frac = (c + 1).astype(np.float64) / 16.0        # exact: k / 16, k = 1..16
+    return fp16_bits_from_float64(frac * m[None, :])
+
+
+def dequant_exl2_qscale(qweight, seg_word_off, bits, q_scale, scale_max, perm, cols=None) -> np.ndarray:
+    """fp16 bits of W [K, N'] in ORIGINAL row order from packed EXL2 with
+    two-level scales: the segment scales of exl2_two_level_scales, then the
+    fp16-scale definition of dequant_exl2."""
+    q_scale = np.asarray(q_scale, dtype=np.uint32)
+    N = q_scale.shape[1] * 8
+    s = exl2_two_level_scales(unpack_exl2_qscale(q_scale, N), scale_max)
+    return dequant_exl2(qweight, seg_word_off, bits, s, perm, cols=cols)
 
 
 # ----------------------------------------------------------------------------

@@ -22,6 +22,8 @@ average bits per weight with bit widths 2/3/4/5/6/8):
   total number of bits is exactly ``bpw * S``; q ~ U{0..2^b-1}; scale
   s ~ U(0.002, 0.03) per (segment, column); a random permutation of the K
   input features.
+* EXL2 with two-level scales: a 4-bit group-scale code c ~ U{0..15} per
+  (segment, column) and a column maximum m ~ U(0.02, 0.05) in fp16.
 * x ~ N(0, 1) in fp16.
 """
 from __future__ import annotations
@@ -31,7 +33,7 @@ from dataclasses import dataclass
 import numpy as np
 
 # Tensor ids inside one layer's seed sequence.
-_T_Q, _T_Z, _T_S, _T_GIDX, _T_BITS, _T_PERM, _T_X = range(7)
+_T_Q, _T_Z, _T_S, _T_GIDX, _T_BITS, _T_PERM, _T_X, _T_QSC, _T_SMAX = range(9)
 
 # Workload ids, so that different workloads draw independent streams.
 WORKLOAD_IDS = {
@@ -206,6 +208,15 @@ def exl2_layer(K: int, N: int, bpw: float = 4.0, allowed=EXL2_BITS, permute: boo
     s = fp16_uniform(rng_for(seed, workload, layer, _T_S), s_range[0], s_range[1], (S, N))
     perm = rng_for(seed, workload, layer, _T_PERM).permutation(K).astype(np.int32) if permute else None
     return Exl2Inputs(q=q, bits=bits, s=s, perm=perm)
+
+
+def exl2_qscale_draws(S: int, N: int, seed: int = 0, workload: int = 99, layer: int = 0,
+                      m_range=(0.02, 0.05)):
+    """Two-level EXL2 scale inputs: codes uint8 [S, N] ~ U{0..15} and column
+    maxima fp16 [N] ~ U(m_range)."""
+    codes = rng_for(seed, workload, layer, _T_QSC).integers(0, 16, size=(S, N)).astype(np.uint8)
+    m = fp16_uniform(rng_for(seed, workload, layer, _T_SMAX), m_range[0], m_range[1], (N,))
+    return codes, m
 
 
 def uniform_words(n_words: int, seed: int = 0, workload: int = 4, layer: int = 0) -> np.ndarray:

@@ -423,3 +423,63 @@ def test_bit_mix_is_exact():
         bits = synth.solve_bit_mix(S, bpw, allowed, np.random.default_rng(S))
         assert int(bits.astype(int).sum()) == int(bpw * S)
         assert set(np.unique(bits).tolist()) <= set(allowed)
+
+
+# ---------------------------------------------------------------- EXL2 two-level scales
+
+def test_exl2_qscale_golden():
+    # hand-derived effective scales, including ties, subnormals and the largest finite value
+    for row in _fixture("exl2_qscale.txt"):
+        m_hex, c, want = row.split()
+        m = np.array([int(m_hex, 16)], dtype=np.uint16)
+        got = int(O.exl2_two_level_scales(np.array([[int(c)]], np.uint8), m)[0, 0])
+        assert got == int(want, 16), (m_hex, c, hex(got), want)
+
+
+def test_exl2_qscale_matches_exact_rational_rounding():
+    # every code against every fp16 maximum of a few binades (normal and
+    # subnormal, both signs): the exact rational (c + 1) / 16 * m rounded by
+    # Python's own binary16 conversion (struct 'e')
+    hs = np.concatenate([np.arange(0x0000, 0x0800, 7), np.arange(0x2C00, 0x3C00, 13), np.arange(0x7800, 0x7C00, 11),
+                         np.arange(0x8001, 0x8400, 17)]).astype(np.uint16)
+    codes = np.arange(16, dtype=np.uint8)[:, None].repeat(hs.size, axis=1)
+    got = O.exl2_two_level_scales(codes, hs)
+    mv = O.float64_from_fp16_bits(hs)
+    for c in range(16):
+        want = [_py_half_bits(float(Fraction(c + 1, 16) * Fraction(float(v)))) for v in mv]
+        assert np.array_equal(got[c], np.array(want, dtype=np.uint16)), c
+
+
+def test_exl2_qscale_packing():
+    # nibble i of word k is column 8k + i: columns 0..7 = 1..8 -> 0x87654321
+    codes = np.zeros((2, 16), dtype=np.uint8)
+    codes[0, :8] = np.arange(1, 9)
+    codes[1, 8:] = 15
+    w = O.pack_exl2_qscale(codes)
+    assert w.tolist() == [[0x87654321, 0], [0, 0xFFFFFFFF]]
+    # the same layout as the GPTQ zero points, packed by another function
+    rng = np.random.default_rng(3)
+    c = rng.integers(0, 16, size=(4, 40)).astype(np.uint8)
+    q = np.zeros((4 * 32, 40), dtype=np.uint8)
+    _, qz, _, _ = O.pack_gptq(q, c, np.ones((4, 40), np.float16), None, 32)
+    assert np.array_equal(O.pack_exl2_qscale(c), qz)
+    assert np.array_equal(O.unpack_exl2_qscale(O.pack_exl2_qscale(c), 40), c)
+    with pytest.raises(ValueError):
+        O.pack_exl2_qscale(np.full((1, 8), 16, np.uint8))
+
+
+def test_exl2_qscale_dequant_reduces_to_fp16_scales():
+    # with the effective scales rounded by numpy, the two-level format is the
+    # fp16-scale format; with every code 15 the scale is the column maximum
+    inp = synth.exl2_layer(256, 48, bpw=4.0, seed=8)
+    codes, m = synth.exl2_qscale_draws(8, 48, seed=8)
+    qw, off, _, perm = O.pack_exl2(inp.q, inp.bits, inp.s, inp.perm)
+    qs = O.pack_exl2_qscale(codes)
+    s_np = (m.astype(np.float64)[None, :] * (codes.astype(np.float64) + 1) / 16).astype(np.float16)
+    W = O.dequant_exl2_qscale(qw, off, inp.bits, qs, m, perm)
+    assert np.array_equal(W, O.dequant_exl2_definitional(inp.q, inp.bits, s_np, inp.perm))
+    top = O.pack_exl2_qscale(np.full((8, 48), 15, np.uint8))
+    W_top = O.dequant_exl2_qscale(qw, off, inp.bits, top, m, perm)
+    assert np.array_equal(W_top, O.dequant_exl2_definitional(inp.q, inp.bits, np.tile(m, (8, 1)), inp.perm))
+    cols = np.array([0, 9, 47])
+    assert np.array_equal(O.dequant_exl2_qscale(qw, off, inp.bits, qs, m, perm, cols=cols), W[:, cols])

@@ -3,7 +3,7 @@
  *
  *   y[M, N] = x[M, K] . dequant(Wq)[K, N]      fp16 in, fp32 accumulate, fp16 out
  *
- * Two weight formats, as described by the ExLlamaV2 pages:
+ * Three weight formats, as described by the ExLlamaV2 pages:
  *
  *  GPTQ 4-bit: group-wise codes q in 0..15, one fp16 scale s and one 4-bit
  *    zero z per (group, output column), w = (q - z) * s. Optional act-order:
@@ -19,6 +19,16 @@
  *    to input features. (ExLlamaV2 README, section "EXL2 quantization";
  *    blog post, "Step 3: Quantization Application".)
  *
+ *  EXL2 with two-level scales: as EXL2, but the scale of (segment, column)
+ *    is a 4-bit code c times the column's fp16 maximum m (the q_scale and
+ *    q_scale_max tensors of the blog post's "Step 3: Quantization
+ *    Application", multiplied together in "How the Fused CUDA Kernel
+ *    Works"). The pages leave the code -> fraction map open; here code c is
+ *    the fraction (c + 1) / 16, so c = 15 is the maximum, and the segment's
+ *    fp16 scale is s = fp16_round_to_nearest_even(((c + 1) / 16) * m), then
+ *    w = (q - 2^(b-1)) * s as for EXL2. Scale storage drops from 16 to 4 bits
+ *    per (segment, column).
+ *
  * Packed layouts (fixed by this library; the pages leave them open):
  *  - qweight is uint32 [n_word_rows, N], N contiguous (row-major), packing
  *    runs along K, least-significant bits first.
@@ -30,6 +40,8 @@
  *    segment's 32 codes form a 32*b-bit stream, code i at stream bits
  *    [i*b, i*b+b), stream bit p is bit (p mod 32) of word row
  *    seg_word_off[s] + p/32. scales fp16 [S, N].
+ *  - EXL2 two-level: q_scale is uint32 [S, N/8], the code of column
+ *    n = 8k + i is nibble i of q_scale[s][k]; q_scale_max fp16 [N].
  *  - perm int32 [K] (optional): perm[j] = input feature (row of x's K axis
  *    and of the dequantized W) held by stored row j.
  *  - Dequantized weight: w = fp16_round_to_nearest_even((q - z) * s), computed
@@ -69,7 +81,7 @@ typedef enum {
   EXQ_ERR_TIMEOUT = 4      /* a device-side wait gave up (from the device)  */
 } exq_status;
 
-typedef enum { EXQ_FMT_GPTQ4 = 1, EXQ_FMT_EXL2 = 2 } exq_format;
+typedef enum { EXQ_FMT_GPTQ4 = 1, EXQ_FMT_EXL2 = 2, EXQ_FMT_EXL2_QSCALE = 3 } exq_format;
 
 /* Plain descriptor of one packed linear layer. Every pointer is a borrowed
  * DEVICE pointer. */
@@ -81,10 +93,12 @@ typedef struct {
   int32_t n_groups;    /* GPTQ: G = K / group_size; EXL2: S = K / 32           */
   int32_t n_word_rows; /* rows of qweight: GPTQ K / 8; EXL2 sum of widths     */
   const uint32_t* qweight;      /* [n_word_rows, N]                           */
-  const uint16_t* scales;       /* fp16 [n_groups, N]                         */
+  const uint16_t* scales;       /* fp16 [n_groups, N]; EXL2 two-level: NULL   */
   const uint32_t* qzeros;       /* GPTQ: [G, N/8]; EXL2: NULL                 */
   const int32_t* perm;          /* [K] stored row -> input feature, or NULL   */
-  const uint32_t* seg_word_off; /* EXL2: [S + 1] word-row prefix sums; GPTQ: NULL */
+  const uint32_t* seg_word_off; /* EXL2 (both): [S + 1] word-row prefix sums; GPTQ: NULL */
+  const uint32_t* q_scale;      /* EXL2 two-level: [S, N/8] 4-bit codes; else NULL */
+  const uint16_t* q_scale_max;  /* EXL2 two-level: fp16 [N] column maxima; else NULL */
 } exq_weight;
 
 /* ---------------------------------------------------------------- packers */
@@ -119,6 +133,15 @@ exq_status exq_pack_gptq(const uint8_t* q, const uint8_t* z, const int32_t* g_id
  * outside the set or a code that does not fit its width. */
 exq_status exq_pack_exl2(const uint8_t* q, const uint8_t* bits, int32_t K, int32_t N,
                          uint32_t* qweight_out, uint32_t* seg_word_off_out);
+
+/* exq_pack_exl2_qscale -- host-only, synchronous, no CUDA.
+ * Packs the 4-bit scale codes of an EXL2 two-level layer.
+ *   codes  [S, N] uint8 codes 0..15, one per (segment, output column) (host)
+ *   q_scale_out [S, N/8] uint32 (host, caller-allocated): nibble i of word k
+ *          is the code of column 8k + i.
+ * Returns EXQ_ERR_INVALID_ARG for NULL buffers, S <= 0, N <= 0, N % 8 or a
+ * code above 15. */
+exq_status exq_pack_exl2_qscale(const uint8_t* codes, int32_t S, int32_t N, uint32_t* q_scale_out);
 
 /* Number of qweight rows an EXL2 layer needs: sum of bits[0..n_segments).
  * Returns -1 if bits is NULL, n_segments <= 0 or a width is outside the set. */

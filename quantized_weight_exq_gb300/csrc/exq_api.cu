@@ -59,13 +59,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 exq_status check_weight(const exq_weight* w) {
   if (!w) return EXQ_ERR_INVALID_ARG;
   if (w->K <= 0 || w->N <= 0 || w->N % 8 || w->K % 32) return EXQ_ERR_INVALID_ARG;
-  if (!w->qweight || !w->scales || !aligned16(w->qweight) || !aligned16(w->scales)) return EXQ_ERR_INVALID_ARG;
+  if (!w->qweight || !aligned16(w->qweight)) return EXQ_ERR_INVALID_ARG;
   if (w->perm && !aligned16(w->perm)) return EXQ_ERR_INVALID_ARG;
+  // fp16 scales, or (EXL2 two-level) codes and column maxima instead
+  const bool two_level = w->format == EXQ_FMT_EXL2_QSCALE;
+  if (two_level) {
+    if (w->scales || !w->q_scale || !w->q_scale_max || !aligned16(w->q_scale) || !aligned16(w->q_scale_max))
+      return EXQ_ERR_INVALID_ARG;
+  } else {
+    if (!w->scales || !aligned16(w->scales) || w->q_scale || w->q_scale_max) return EXQ_ERR_INVALID_ARG;
+  }
   if (w->format == EXQ_FMT_GPTQ4) {
     if (w->group_size <= 0 || w->group_size % 32 || w->K % w->group_size) return EXQ_ERR_INVALID_ARG;
     if (w->n_groups != w->K / w->group_size || w->n_word_rows != w->K / 8) return EXQ_ERR_INVALID_ARG;
     if (!w->qzeros || !aligned16(w->qzeros) || w->seg_word_off) return EXQ_ERR_INVALID_ARG;
-  } else if (w->format == EXQ_FMT_EXL2) {
+  } else if (w->format == EXQ_FMT_EXL2 || two_level) {
     if (w->group_size != 32 || w->n_groups != w->K / 32) return EXQ_ERR_INVALID_ARG;
     if (w->n_word_rows < 2 * w->n_groups || w->n_word_rows > 8 * w->n_groups) return EXQ_ERR_INVALID_ARG;
     if (!w->seg_word_off || w->qzeros) return EXQ_ERR_INVALID_ARG;

@@ -24,6 +24,8 @@ constexpr int kThreads = kWarps * 32;
 struct DequantArgs {
   const uint32_t* qweight;
   const uint16_t* scales;
+  const uint32_t* q_scale;      // EXL2 two-level codes [S, N / 8]
+  const uint16_t* q_scale_max;  // EXL2 two-level column maxima [N]
   const uint32_t* qzeros;
   const int32_t* perm;
   const uint32_t* seg_off;
@@ -106,7 +108,17 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const __grid_constant
         wb[1] = ld_stream(a.qweight + (row + 1) * a.N + col + 4);
       }
     }
-    sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<size_t>(s) * a.N + col));
+    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
+      // the 8 columns' codes are one word; their maxima one 16-byte vector
+      const uint32_t cw = __ldg(a.q_scale + static_cast<size_t>(s) * (a.N >> 3) + (col >> 3));
+      const uint4 mv = __ldg(reinterpret_cast<const uint4*>(a.q_scale_max + col));
+      sv.x = two_level_scale2((cw & 0xFFu) | ((cw & 0xF0u) << 12), mv.x);
+      sv.y = two_level_scale2(((cw >> 8) & 0xFFu) | ((cw & 0xF000u) << 4), mv.y);
+      sv.z = two_level_scale2(((cw >> 16) & 0xFFu) | ((cw >> 4) & 0xF0000u), mv.z);
+      sv.w = two_level_scale2((cw >> 24) | ((cw >> 12) & 0xF0000u), mv.w);
+    } else {
+      sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<size_t>(s) * a.N + col));
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint32_t h = comp8(sv, sv, c >> 1);
@@ -162,6 +174,8 @@ exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t str
   DequantArgs args{};
   args.qweight = w.qweight;
   args.scales = w.scales;
+  args.q_scale = w.q_scale;
+  args.q_scale_max = w.q_scale_max;
   args.qzeros = w.qzeros;
   args.perm = w.perm;
   args.seg_off = w.seg_word_off;
@@ -176,9 +190,12 @@ exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t str
   if (w.format == EXQ_FMT_GPTQ4) {
     if (perm) dequant_kernel<EXQ_FMT_GPTQ4, true><<<grid, kThreads, 0, stream>>>(args);
     else dequant_kernel<EXQ_FMT_GPTQ4, false><<<grid, kThreads, 0, stream>>>(args);
-  } else {
+  } else if (w.format == EXQ_FMT_EXL2) {
     if (perm) dequant_kernel<EXQ_FMT_EXL2, true><<<grid, kThreads, 0, stream>>>(args);
     else dequant_kernel<EXQ_FMT_EXL2, false><<<grid, kThreads, 0, stream>>>(args);
+  } else {
+    if (perm) dequant_kernel<EXQ_FMT_EXL2_QSCALE, true><<<grid, kThreads, 0, stream>>>(args);
+    else dequant_kernel<EXQ_FMT_EXL2_QSCALE, false><<<grid, kThreads, 0, stream>>>(args);
   }
   if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
   return EXQ_OK;

@@ -91,8 +91,8 @@ constexpr int kSplitSmBound = 256;  // SM count the workspace bound allows for
 struct GemmMaps {
   CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 128, 128-byte swizzle
   CUtensorMap w[6];  // qweight [rows, N] uint32, boxes 256 columns x b rows, b in {2,3,4,5,6,8}
-  CUtensorMap s;     // scales [groups, N] fp16, boxes 256 x 1
-  CUtensorMap z;     // GPTQ zeros [groups, N / 8] uint32, boxes 32 x 1
+  CUtensorMap s;     // scales [groups, N] fp16, boxes 128 x 1 (unused with two-level scales)
+  CUtensorMap z;     // GPTQ zeros or two-level scale codes [groups, N / 8] uint32, boxes 16 x 1
 };
 
 // tensor map of a box of b word rows
@@ -100,6 +100,7 @@ __device__ __forceinline__ int wmap_index(int b) { return b == 8 ? 5 : b - 2; }
 
 struct GemmArgs {
   const uint32_t* seg_off;
+  const uint16_t* q_scale_max;  // EXL2 two-level column maxima [N]
   uint16_t* y;
   float* part;      // [split, M, N] fp32 partial sums when split > 1
   int M, N, K, gs, n_word_rows;
@@ -357,8 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[s].rows1 = rows1;
         const int rows = rows0 + rows1;
         // boxes always move their full size (rows past M and columns past N read as zero)
-        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u + 2u * BN * 2u;
-        if constexpr (FMT == EXQ_FMT_GPTQ4) tx += 2u * (BN / 8) * 4u;
+        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u;
+        if constexpr (FMT != EXQ_FMT_EXL2_QSCALE) tx += 2u * BN * 2u;  // fp16 scale rows
+        if constexpr (FMT != EXQ_FMT_EXL2) tx += 2u * (BN / 8) * 4u;   // zero or scale-code rows
         mbar_expect_tx(bar, tx);
         tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
@@ -370,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int h = 0; h < 2; ++h) {
           const int g = FMT == EXQ_FMT_GPTQ4 ? (kt * BK + 32 * h) / a.gs : 2 * kt + h;
-          tma_load_2d(smem_u32(st + kOffScale + h * BN * 2), &maps.s, n0, g, bar);
-          if constexpr (FMT == EXQ_FMT_GPTQ4)
+          if constexpr (FMT != EXQ_FMT_EXL2_QSCALE)
+            tma_load_2d(smem_u32(st + kOffScale + h * BN * 2), &maps.s, n0, g, bar);
+          if constexpr (FMT != EXQ_FMT_EXL2)
             tma_load_2d(smem_u32(st + kOffZero + h * kZeroStride), &maps.z, n0 / 8, g, bar);
         }
         issued = i + 1;
@@ -408,6 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp - 2) >> 2;               // its 32-row half of the slab
     const int col = q * 32 + lane;               // output column in the tile = A row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    // two-level scales: this column's fp16 maximum, in both halves
+    uint32_t m2 = 0u;
+    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
+      const uint32_t m = __ldg(a.q_scale_max + n0 + col);
+      m2 = m | (m << 16);
+    }
     for (int i = 0; i < n_iter; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
@@ -416,9 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint8_t* st = smem + s * kStageBytes;
       const uint32_t* packed = reinterpret_cast<const uint32_t*>(st + kOffPacked);
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
-      const uint32_t s16 = sc[h * BN + col];
-      const uint32_t s2 = s16 | (s16 << 16);
+      uint32_t s2;
+      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
+        // s = fp16_RN(((c + 1) / 16) m) from the column's 4-bit code
+        const uint32_t cw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
+        const uint32_t c = (cw >> (4 * (col & 7))) & 0xFu;
+        s2 = two_level_scale2(c | (c << 16), m2);
+      } else {
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
+        const uint32_t s16 = sc[h * BN + col];
+        s2 = s16 | (s16 << 16);
+      }
       uint32_t r[16];
       if constexpr (FMT == EXQ_FMT_GPTQ4) {
         const uint32_t zw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
@@ -634,7 +651,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return EXQ_ERR_CUDA;
   }
-  {
+  if (w.scales) {
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_groups)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 2};
     const cuuint32_t box[2] = {BN, 1};
@@ -643,11 +660,12 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return EXQ_ERR_CUDA;
   }
-  if (w.format == EXQ_FMT_GPTQ4) {
+  if (w.format != EXQ_FMT_EXL2) {  // GPTQ zeros or two-level scale codes
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N / 8), static_cast<cuuint64_t>(w.n_groups)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N / 8) * 4};
     const cuuint32_t box[2] = {BN / 8, 1};
-    if (enc(&maps.z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qzeros), gdim, gstride, box, es,
+    const uint32_t* zsrc = w.format == EXQ_FMT_GPTQ4 ? w.qzeros : w.q_scale;
+    if (enc(&maps.z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(zsrc), gdim, gstride, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return EXQ_ERR_CUDA;
@@ -655,6 +673,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
 
   GemmArgs args{};
   args.seg_off = w.seg_word_off;
+  args.q_scale_max = w.q_scale_max;
   args.y = y;
   args.part = part;
   args.M = M;
@@ -665,9 +684,11 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   args.split = plan.split;
   args.slabs_per = plan.slabs_per;
 
-  auto fn = w.format == EXQ_FMT_GPTQ4 ? gemm_kernel<EXQ_FMT_GPTQ4> : gemm_kernel<EXQ_FMT_EXL2>;
-  static std::once_flag attr_once[2];
-  std::call_once(attr_once[w.format == EXQ_FMT_GPTQ4 ? 0 : 1],
+  auto fn = w.format == EXQ_FMT_GPTQ4 ? gemm_kernel<EXQ_FMT_GPTQ4>
+            : w.format == EXQ_FMT_EXL2  ? gemm_kernel<EXQ_FMT_EXL2>
+                                        : gemm_kernel<EXQ_FMT_EXL2_QSCALE>;
+  static std::once_flag attr_once[3];
+  std::call_once(attr_once[w.format - 1],
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
   {
     cudaLaunchConfig_t cfg{};

@@ -42,6 +42,10 @@
 //    and no warp ever waits on another CTA.
 //  * An act-order layer's x is gathered into stored-row order by a small
 //    kernel first (into the workspace), once per call rather than per CTA.
+//  * EXL2 with two-level scales: instead of the scale box, the stage's rows
+//    of 4-bit scale codes follow as 4-byte asynchronous copies (like GPTQ
+//    zeros) and the tile's fp16 column maxima as one 16-byte copy per lane;
+//    the consumers form each segment's scales as fp16_RN(((c + 1) / 16) m).
 //  * Programmatic dependent launch: every kernel lets the next launch start
 //    early; the GEMV's first weight copies do not wait for the previous
 //    kernel, its activations and outputs do.
@@ -101,6 +105,8 @@ struct GemvMaps {
 struct GemvLayer {
   const uint32_t* seg_off;  // EXL2 [S + 1]
   const uint32_t* qzeros;   // GPTQ [G, N / 8]
+  const uint32_t* q_scale;  // EXL2 two-level codes [S, N / 8]
+  const uint16_t* q_scale_max;  // EXL2 two-level column maxima [N]
   uint16_t* y;              // [M, N]
   int N;
   int n_word_rows;
@@ -216,6 +222,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -291,6 +300,18 @@ __device__ __forceinline__ void scales4(const uint8_t* p, uint32_t (&s2)[4]) {
   s2[1] = prmt(v.x, v.x, 0x3232);
   s2[2] = prmt(v.y, v.y, 0x1010);
   s2[3] = prmt(v.y, v.y, 0x3232);
+}
+
+// the same from two-level scales: `codes` = the lane's four 4-bit codes in
+// its low 16 bits, mv = the four columns' fp16 maxima
+__device__ __forceinline__ void qscales4(uint32_t codes, const uint2& mv, uint32_t (&s2)[4]) {
+  const uint32_t lo = codes & 0xFFFFu, hi = lo >> 8;
+  const uint32_t a = two_level_scale2(lo | (lo << 12), mv.x);  // columns 0, 1
+  const uint32_t b = two_level_scale2(hi | (hi << 12), mv.y);  // columns 2, 3
+  s2[0] = prmt(a, a, 0x1010);
+  s2[1] = prmt(a, a, 0x3232);
+  s2[2] = prmt(b, b, 0x1010);
+  s2[3] = prmt(b, b, 0x3232);
 }
 
 // w = fp16_RN((q - z) s) for the lane's four columns
@@ -420,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int l = 0; l < kMaxLayers; ++l)
         if (l >= la && l <= lb) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w[l])) : "memory");
-          asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.s[l])) : "memory");
+          if constexpr (FMT != EXQ_FMT_EXL2_QSCALE)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.s[l])) : "memory");
         }
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
     }
-    if constexpr (FMT == EXQ_FMT_EXL2) {
+    if constexpr (FMT != EXQ_FMT_GPTQ4) {
       // the segment tables are model state: copy them before the wait
 #pragma unroll
       for (int l = 0; l < kMaxLayers; ++l)
@@ -434,13 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXRowBytes;
-    const uint32_t tx = kRowsPerStage * kTN * 4 + kScaleRows * kTN * 2 + x_bytes;
+    // two-level scales arrive by cp.async, not in the transaction count
+    const uint32_t tx = kRowsPerStage * kTN * 4 + (FMT == EXQ_FMT_EXL2_QSCALE ? 0 : kScaleRows * kTN * 2) + x_bytes;
     int slot = 0, ephase = 0, issued = 0, npend = 0;
     // the piece's layer: its index, tensor maps, first row of x, GPTQ zeros
     const CUtensorMap* mw = &maps.w[0];
     const CUtensorMap* ms = &maps.s[0];
-    int layer = 0, xrow = 0, nz = 0;
-    const uint32_t* qz = nullptr;
+    int layer = 0, xrow = 0, nz = 0, ncols = 0;  // ncols: the tile's columns (two-level maxima)
+    const uint32_t* qz = nullptr;                // GPTQ zeros or two-level scale codes
+    const uint16_t* qmax = nullptr;
     bool waited = false, ok = true;
     auto release_x = [&]() {  // the activations may be read once the previous kernel is done
       asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -462,14 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0)
         desc[slot] = Desc{da, widths, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16),
                           static_cast<uint32_t>(srow)};
-      if constexpr (FMT == EXQ_FMT_GPTQ4) {
+      if constexpr (FMT != EXQ_FMT_EXL2) {
         if (!bad) {
+          // GPTQ zero rows or two-level scale-code rows: [rows, N / 8] words
           const int cw = lt * (kTN / 8) + lane;
 #pragma unroll
           for (int r = 0; r < kScaleRows; ++r)
             if (srow + r < a.G && cw < nz && lane < kTN / 8)
               cp_async4(smem_u32(st + kSlotZ + r * kZeroRowBytes + lane * 4),
                         qz + static_cast<size_t>(srow + r) * nz + cw);
+          // two-level: the tile's column maxima, 8 columns (16 bytes) per lane
+          if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+            if (8 * lane < ncols) cp_async16(smem_u32(st + kSlotS + 16 * lane), qmax + lt * kTN + 8 * lane);
           cp_async_arrive(fb);  // one more pending arrival, made when this lane's copies land
         }
       }
@@ -480,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_expect_tx(fb, tx);
           tma_load_2d(smem_u32(st + kSlotW), mw, lt * kTN, row0, fb);
-          tma_load_2d(smem_u32(st + kSlotS), ms, lt * kTN, srow, fb);
+          if constexpr (FMT != EXQ_FMT_EXL2_QSCALE) tma_load_2d(smem_u32(st + kSlotS), ms, lt * kTN, srow, fb);
           if (waited) tma_load_2d(smem_u32(st + kSlotX), &maps.x, static_cast<int>(da & 0xFFFFu) * 32, xrow, fb);
         }
       }
@@ -501,8 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mw = &maps.w[layer];
       ms = &maps.s[layer];
       xrow = ly.x_row;
-      qz = ly.qzeros;
+      qz = FMT == EXQ_FMT_EXL2_QSCALE ? ly.q_scale : ly.qzeros;
+      qmax = ly.q_scale_max;
       nz = ly.N / 8;
+      ncols = min(kTN, ly.N - lt * kTN);
       const int sa = u - tile * a.S;
       const int sb = min(a.S, sa + (u1 - u));
       u += sb - sa;
@@ -518,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           srow = seg / a.gs_seg;
         } else {
           // greedy, one candidate segment per lane: the longest run of valid
-          // segments from seg (at most four) whose widths add up to at most 16
+          // segments from seg (at most eight) whose widths add up to at most 32
           const int sk = seg + lane;
           const bool cand = lane < kSegsPerStage && sk < sb;
           const uint32_t* ltbl = tbl + layer * (a.S + 1);
@@ -602,8 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_off = 64 * w + 8 * g;  // byte offset of the lane's 4 scales in a scale row
     const int h = (n + 1) >> 1;
     const int j0 = kg ? h : 0, j1 = kg ? n : h;  // this K group's segments of the stage
-    if constexpr (FMT == EXQ_FMT_EXL2) {
+    if constexpr (FMT != EXQ_FMT_GPTQ4) {
       const uint32_t widths = d.b;
+      // two-level: the lane's four column maxima (the same for every segment of the tile)
+      uint2 mv = make_uint2(0u, 0u);
+      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) mv = lds64(sl + kSlotS + col_off);
       int o = kg ? static_cast<int>(d.a >> 24) : 0;  // word row of segment j0 in the slot
       for (int j = j0; j < j1; ++j) {
         const int b = static_cast<int>((widths >> (4 * j)) & 15u);
@@ -611,7 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t xb[MT][4];
           x_pairs(xrow0 + 64 * j, xb[0]);
           if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
-          scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
+          if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+            qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
+          else
+            scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
           const int bit = 8 * t * b;
           const uint8_t* row = wrow + (o + (bit >> 5)) * kRowBytes;
           const uint32_t off = static_cast<uint32_t>(bit & 31);
@@ -732,10 +768,12 @@ KernelFn pick_for(int M) {
 }
 
 KernelFn pick_kernel(int fmt, int M) {
-  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4>(M) : pick_for<EXQ_FMT_EXL2>(M);
+  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4>(M)
+         : fmt == EXQ_FMT_EXL2 ? pick_for<EXQ_FMT_EXL2>(M)
+                               : pick_for<EXQ_FMT_EXL2_QSCALE>(M);
 }
 
-int variant_index(int fmt, int M) { return (fmt == EXQ_FMT_GPTQ4 ? 0 : 2) + (M <= 8 ? 0 : 1); }
+int variant_index(int fmt, int M) { return 2 * (fmt - 1) + (M <= 8 ? 0 : 1); }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -775,7 +813,7 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
   }
   p.G = std::max(1, std::min(G, p.total));
   p.slot_bytes = slot_bytes_for(M);
-  const size_t table = w[0].format == EXQ_FMT_EXL2 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
+  const size_t table = w[0].format != EXQ_FMT_GPTQ4 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
   const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment tables, alignment slack
   const long long room = static_cast<long long>(kSmemPerCta) - static_cast<long long>(fixed);
   p.stages = static_cast<int>(std::min<long long>(kMaxStages, room / p.slot_bytes));
@@ -793,7 +831,7 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
 }
 
 std::mutex g_attr_mutex;
-bool g_attr_done[64][4];
+bool g_attr_done[64][6];
 
 }  // namespace
 
@@ -873,12 +911,16 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
       continue;
     }
     if (!encode_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[i].qweight, w[i].N, w[i].n_word_rows,
-                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage) ||
-        !encode_2d(&maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, w[i].scales, w[i].N, scale_rows,
-                   static_cast<uint64_t>(w[i].N) * 2, kTN, kScaleRows))
+                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage))
+      return EXQ_ERR_CUDA;
+    // fp16 scale rows (two-level scales come without a tensor map)
+    if (w[i].scales && !encode_2d(&maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, w[i].scales, w[i].N, scale_rows,
+                                  static_cast<uint64_t>(w[i].N) * 2, kTN, kScaleRows))
       return EXQ_ERR_CUDA;
     l.seg_off = w[i].seg_word_off;
     l.qzeros = w[i].qzeros;
+    l.q_scale = w[i].q_scale;
+    l.q_scale_max = w[i].q_scale_max;
     l.y = y[i];
     l.N = w[i].N;
     l.n_word_rows = w[i].n_word_rows;

@@ -111,3 +111,20 @@ extern "C" exq_status exq_pack_exl2(const uint8_t* q, const uint8_t* bits, int32
   seg_word_off_out[S] = off;
   return EXQ_OK;
 }
+
+// Two-level EXL2 scale codes: eight 4-bit codes per word along N, least
+// significant nibble first (the layout of the GPTQ zero points).
+extern "C" exq_status exq_pack_exl2_qscale(const uint8_t* codes, int32_t S, int32_t N, uint32_t* q_scale_out) {
+  if (!codes || !q_scale_out || S <= 0 || N <= 0 || N % 8) return EXQ_ERR_INVALID_ARG;
+  for (int64_t s = 0; s < S; ++s)
+    for (int32_t k = 0; k < N / 8; ++k) {
+      uint32_t word = 0;
+      for (int i = 0; i < 8; ++i) {
+        const uint8_t v = codes[s * N + 8 * k + i];
+        if (v > 15) return EXQ_ERR_INVALID_ARG;
+        word |= static_cast<uint32_t>(v) << (4 * i);
+      }
+      q_scale_out[s * (N / 8) + k] = word;
+    }
+  return EXQ_OK;
+}

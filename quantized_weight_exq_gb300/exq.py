@@ -25,10 +25,11 @@ EXQ_ERR_TIMEOUT = 4
 
 EXQ_FMT_GPTQ4 = 1
 EXQ_FMT_EXL2 = 2
+EXQ_FMT_EXL2_QSCALE = 3
 
 # every symbol include/exq.h declares
 EXPORTED = (
-    "exq_pack_gptq", "exq_pack_exl2", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
+    "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
     "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error",
 )
@@ -52,6 +53,7 @@ class exq_weight(ctypes.Structure):
         ("group_size", ctypes.c_int32), ("n_groups", ctypes.c_int32), ("n_word_rows", ctypes.c_int32),
         ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("qzeros", ctypes.c_void_p),
         ("perm", ctypes.c_void_p), ("seg_word_off", ctypes.c_void_p),
+        ("q_scale", ctypes.c_void_p), ("q_scale_max", ctypes.c_void_p),
     ]
 
 
@@ -65,6 +67,7 @@ def _load():
     sig = {
         "exq_pack_gptq": (st, [P, P, P, i32, i32, i32, P, P, P]),
         "exq_pack_exl2": (st, [P, P, i32, i32, P, P]),
+        "exq_pack_exl2_qscale": (st, [P, i32, i32, P]),
         "exq_exl2_word_rows": (i64, [P, i32]),
         "exq_dequant": (st, [W, P, P]),
         "exq_gemv_workspace_size": (sz, [W, i32]),
@@ -151,6 +154,15 @@ def exq_pack_exl2(q: np.ndarray, bits: np.ndarray):
     return qweight, off
 
 
+def exq_pack_exl2_qscale(codes: np.ndarray) -> np.ndarray:
+    """4-bit scale codes uint8 [S, N] -> q_scale uint32 [S, N/8]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    S, N = codes.shape
+    out = np.empty((S, max(N // 8, 1)), dtype=np.uint32)
+    _check(_lib.exq_pack_exl2_qscale(_np_ptr(codes), S, N, _np_ptr(out)), "exq_pack_exl2_qscale")
+    return out
+
+
 # ---------------------------------------------------------------- device layer
 
 @dataclass
@@ -162,26 +174,32 @@ class Weight:
     N: int
     group_size: int
     qweight: "object"                 # torch.int32 [rows, N] (uint32 bits)
-    scales: "object"                  # torch.float16 [G or S, N]
+    scales: "object"                  # torch.float16 [G or S, N]; None for EXL2 two-level
     qzeros: "object" = None           # torch.int32 [G, N/8] (GPTQ)
     perm: "object" = None             # torch.int32 [K]
     seg_word_off: "object" = None     # torch.int32 [S + 1] (EXL2)
+    q_scale: "object" = None          # torch.int32 [S, N/8] 4-bit codes (EXL2 two-level)
+    q_scale_max: "object" = None      # torch.float16 [N] (EXL2 two-level)
     _desc: exq_weight = field(default=None, repr=False)
 
     def desc(self) -> exq_weight:
         if self._desc is None:
             ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+            groups = self.scales.shape[0] if self.scales is not None else self.q_scale.shape[0]
             self._desc = exq_weight(
-                self.format, self.K, self.N, self.group_size, self.scales.shape[0], self.qweight.shape[0],
-                ptr(self.qweight), ptr(self.scales), ptr(self.qzeros), ptr(self.perm), ptr(self.seg_word_off))
+                self.format, self.K, self.N, self.group_size, groups, self.qweight.shape[0],
+                ptr(self.qweight), ptr(self.scales), ptr(self.qzeros), ptr(self.perm), ptr(self.seg_word_off),
+                ptr(self.q_scale), ptr(self.q_scale_max))
         return self._desc
 
     @property
     def packed_bytes(self) -> int:
-        """qweight + scales + qzeros bytes (the weight stream of one matmul)."""
-        n = self.qweight.numel() * 4 + self.scales.numel() * 2
-        if self.qzeros is not None:
-            n += self.qzeros.numel() * 4
+        """qweight + scales (or scale codes and column maxima) + qzeros bytes:
+        the weight stream of one matmul."""
+        n = self.qweight.numel() * 4
+        for t, size in ((self.scales, 2), (self.qzeros, 4), (self.q_scale, 4), (self.q_scale_max, 2)):
+            if t is not None:
+                n += t.numel() * size
         return n
 
 
@@ -211,6 +229,15 @@ def exl2_weight(qweight, seg_word_off, scales, perm, K: int, N: int, device="cud
     return Weight(EXQ_FMT_EXL2, K, N, 32, _dev(qweight, torch.int32, device),
                   _dev(scales, torch.float16, device), None, _dev(perm, torch.int32, device),
                   _dev(seg_word_off, torch.int32, device))
+
+
+def exl2_qscale_weight(qweight, seg_word_off, q_scale, q_scale_max, perm, K: int, N: int, device="cuda") -> Weight:
+    """EXL2 layer with two-level scales: q_scale uint32 [S, N/8] packed codes
+    (exq_pack_exl2_qscale), q_scale_max fp16 [N]."""
+    import torch
+    return Weight(EXQ_FMT_EXL2_QSCALE, K, N, 32, _dev(qweight, torch.int32, device), None, None,
+                  _dev(perm, torch.int32, device), _dev(seg_word_off, torch.int32, device),
+                  _dev(q_scale, torch.int32, device), _dev(q_scale_max, torch.float16, device))
 
 
 def exq_dequant(w: Weight, W_out, stream=None):

@@ -79,7 +79,8 @@ def test_packers_reject_bad_input(exq):
 
 def _desc(exq, **kw):
     base = dict(format=exq.EXQ_FMT_GPTQ4, K=256, N=64, group_size=128, n_groups=2, n_word_rows=32,
-                qweight=0x10000, scales=0x20000, qzeros=0x30000, perm=None, seg_word_off=None)
+                qweight=0x10000, scales=0x20000, qzeros=0x30000, perm=None, seg_word_off=None,
+                q_scale=None, q_scale_max=None)
     base.update(kw)
     return exq.exq_weight(*[base[f] for f, _ in exq.exq_weight._fields_])
 
@@ -150,3 +151,42 @@ def test_gemv_multi_validates_on_host(exq):
     assert lib.exq_gemv_multi_workspace_size(arr, 2, 17) == 0
     mixed = (exq.exq_weight * 2)(d, exl2)
     assert lib.exq_gemv_multi_workspace_size(mixed, 2, 1) == 0
+
+
+def test_pack_exl2_qscale_matches_oracle(exq):
+    codes, _ = synth.exl2_qscale_draws(12, 40, seed=2)
+    assert np.array_equal(exq.exq_pack_exl2_qscale(codes), O.pack_exl2_qscale(codes))
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_exl2_qscale(np.full((2, 8), 16, np.uint8))   # code > 15
+    with pytest.raises(exq.ExqError):
+        exq.exq_pack_exl2_qscale(np.zeros((2, 12), np.uint8))     # N % 8
+
+
+def test_two_level_descriptor_rules(exq):
+    from quantized_weight_exq_gb300 import exq as mod
+    lib = mod._lib
+    qs = dict(format=exq.EXQ_FMT_EXL2_QSCALE, group_size=32, n_groups=8, n_word_rows=32, qzeros=None,
+              seg_word_off=0x40000, scales=None, q_scale=0x80000, q_scale_max=0x90000)
+    bad = [
+        dict(scales=0x20000),            # fp16 scales as well
+        dict(q_scale=None),              # no codes
+        dict(q_scale_max=None),          # no maxima
+        dict(q_scale=0x80004),           # misaligned codes
+        dict(q_scale_max=0x90002),       # misaligned maxima
+        dict(seg_word_off=None),         # no segment table
+    ]
+    for kw in bad:
+        d = _desc(exq, **{**qs, **kw})
+        assert lib.exq_gemv(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
+        assert lib.exq_dequant(ctypes.byref(d), 0x60000, None) == exq.EXQ_ERR_INVALID_ARG, kw
+        assert lib.exq_gemm(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
+    # codes or maxima on the other formats are rejected too
+    for kw in (dict(q_scale=0x80000), dict(q_scale_max=0x90000)):
+        d = _desc(exq, **kw)
+        assert lib.exq_gemv(ctypes.byref(d), 0x50000, 1, 0x60000, None, 0, None) == exq.EXQ_ERR_INVALID_ARG, kw
+    # a two-level layer and an fp16-scale EXL2 layer do not group
+    e = _desc(exq, format=exq.EXQ_FMT_EXL2, group_size=32, n_groups=8, n_word_rows=32, qzeros=None,
+              seg_word_off=0x40000)
+    arr = (exq.exq_weight * 2)(_desc(exq, **qs), e)
+    yp = (ctypes.c_void_p * 2)(0x60000, 0x61000)
+    assert lib.exq_gemv_multi(arr, 2, 0x50000, 1, yp, None, 0, None) == exq.EXQ_ERR_INVALID_ARG

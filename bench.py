@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--impl", default="exq", choices=["exq", "reference"])
     ap.add_argument("--layers", type=int, default=80, help="decoder layers in the stream (80 = Llama-2-70B)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--format", default="exl2", choices=["exl2", "exl2_qscale"],
+                    help="decode stream format: EXL2 4.0 bpw with fp16 scales (default) or with two-level "
+                         "scales (4-bit group-scale codes x per-column fp16 maxima)")
     ap.add_argument("--ungrouped", action="store_true",
                     help="decode stream as one exq_gemv per linear (each with its own x) instead of grouping "
                          "the linears that share x (q/k/v, gate/up) into exq_gemv_multi calls")
@@ -154,7 +157,7 @@ def bit_mix(layer: int, lin: int, K: int):
     return synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, synth.rng_for(0, wid, 7 * layer + lin, 4))
 
 
-def build_stream(exq, torch, layers: int, device, grouped: bool = True):
+def build_stream(exq, torch, layers: int, device, grouped: bool = True, two_level: bool = False):
     """Device-resident packed weights for the whole stream, as a list of
     calls (weights, x, outputs). Packed codes are uniform random words (a
     segment column's b words are a bijection of its 32 uniform b-bit codes);
@@ -178,15 +181,7 @@ def build_stream(exq, torch, layers: int, device, grouped: bool = True):
                 K, N = synth.LLAMA2_70B_SHAPES[name]
                 gen = torch.Generator(device=device)
                 gen.manual_seed(int(synth.rng_for(0, wid, 7 * layer + i, 0).integers(0, 2 ** 62)))
-                bits = bit_mix(layer, i, K)
-                off = np.zeros(bits.size + 1, dtype=np.int64)
-                off[1:] = np.cumsum(bits.astype(np.int64))
-                rows = int(off[-1])
-                qweight = torch.randint(0, 2 ** 32, (rows, N), dtype=torch.int64, device=device,
-                                        generator=gen).to(torch.int32)
-                scales = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
-                perm = torch.randperm(K, device=device, generator=gen).to(torch.int32)
-                ws.append(exq.exl2_weight(qweight, off.astype(np.int32), scales, perm, K, N, device=device))
+                ws.append(exl2_device_layer(exq, torch, K, N, bit_mix(layer, i, K), gen, device, two_level))
                 if x is None:  # the group's activations: drawn with its first linear's generator
                     x = x_all[xo:xo + K].view(1, K)
                     x.copy_(torch.randn(1, K, device=device, generator=gen).half())
@@ -212,6 +207,26 @@ def call_workspace_size(exq, call) -> int:
     return exq.exq_gemv_multi_workspace_size(ws, x.shape[0])
 
 
+def exl2_device_layer(exq, torch, K, N, bits, gen, device, two_level=False, perm=True):
+    """An EXL2 layer drawn on the device: uniform packed words (the packing is
+    a bijection, so these are uniform codes), fp16 scales ~ U(0.002, 0.03) or
+    two-level scales (uniform 4-bit codes, column maxima ~ U(0.02, 0.05)), and
+    a random permutation."""
+    off = np.zeros(bits.size + 1, dtype=np.int64)
+    off[1:] = np.cumsum(bits.astype(np.int64))
+    qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
+    if two_level:
+        qs = torch.randint(0, 2 ** 32, (K // 32, N // 8), dtype=torch.int64, device=device,
+                           generator=gen).to(torch.int32)
+        mx = (torch.rand(N, device=device, generator=gen) * 0.03 + 0.02).half()
+    else:
+        sc = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
+    pm = torch.randperm(K, device=device, generator=gen).to(torch.int32) if perm else None
+    if two_level:
+        return exq.exl2_qscale_weight(qw, off.astype(np.int32), qs, mx, pm, K, N, device=device)
+    return exq.exl2_weight(qw, off.astype(np.int32), sc, pm, K, N, device=device)
+
+
 PREFILL_SHAPES = (("q", 8192, 8192), ("k", 8192, 1024), ("gate", 8192, 28672), ("down", 28672, 8192))
 
 
@@ -235,8 +250,8 @@ def run_prefill(args, device):
     except Exception:
         peak_bf16 = 1900.0
     shapes = {}
-    for fmt in ("gptq_g128", "exl2_2.5bpw"):
-        for M in (512, 2048):
+    for fmt in ("gptq_g128", "exl2_2.5bpw", "exl2_2.5bpw_two_level"):
+        for M in ((2048,) if fmt.endswith("two_level") else (512, 2048)):
             for name, K, N in PREFILL_SHAPES:
                 gen = torch.Generator(device=device)
                 gen.manual_seed(1000 * M + K + N)
@@ -249,12 +264,8 @@ def run_prefill(args, device):
                     w = exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device)
                 else:
                     bits = synth.solve_bit_mix(K // 32, 2.5, (2, 3, 4), np.random.default_rng(K + N))
-                    off = np.zeros(bits.size + 1, np.int64)
-                    off[1:] = np.cumsum(bits)
-                    qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device,
-                                       generator=gen).to(torch.int32)
-                    sc = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
-                    w = exq.exl2_weight(qw, off.astype(np.int32), sc, None, K, N, device=device)
+                    w = exl2_device_layer(exq, torch, K, N, bits, gen, device,
+                                          two_level=fmt.endswith("two_level"), perm=False)
                 x = torch.randn(M, K, device=device, generator=gen).half()
                 y = torch.empty(M, N, device=device, dtype=torch.float16)
                 nws = exq.exq_gemm_workspace_size(w, M)
@@ -322,15 +333,9 @@ def run_decode_sweep(args, device):
         perm = torch.randperm(K, device=device, generator=gen).int() if act else None
         return exq.gptq_weight(qw, qz, sc, perm, K, N, 128, device=device)
 
-    def exl2(K, N, gen, rng):
+    def exl2(K, N, gen, rng, two_level=False):
         bits = synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, rng)
-        off = np.zeros(bits.size + 1, np.int64)
-        off[1:] = np.cumsum(bits)
-        qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device,
-                           generator=gen).to(torch.int32)
-        sc = (torch.rand(K // 32, N, device=device, generator=gen) * 0.028 + 0.002).half()
-        perm = torch.randperm(K, device=device, generator=gen).int()
-        return exq.exl2_weight(qw, off.astype(np.int32), sc, perm, K, N, device=device)
+        return exl2_device_layer(exq, torch, K, N, bits, gen, device, two_level)
 
     cases = [("gptq_g128 4096x4096", "gptq", 4096, (4096,), False, (1,))]
     for name, (K, N) in synth.LLAMA2_7B_SHAPES.items():
@@ -345,13 +350,18 @@ def run_decode_sweep(args, device):
         tag = "+".join(grp)
         cases.append((f"gptq_act_order 7b {tag} grouped", "gptq", K, Ns, True, (1, 4, 16)))
         cases.append((f"exl2_4.0bpw 7b {tag} grouped", "exl2", K, Ns, True, (1, 8)))
+    # the same EXL2 shapes with two-level scales
+    K, N = synth.LLAMA2_7B_SHAPES["gate"]
+    cases.append((f"exl2_4.0bpw_two_level 7b gate {K}x{N}", "exl2_qs", K, (N,), True, (1, 8)))
+    cases.append(("exl2_4.0bpw_two_level 7b gate+up grouped", "exl2_qs", K, (N, N), True, (1, 8)))
     shapes = {}
     for label, fmt, K, Ns, act, Ms in cases:
         gen = torch.Generator(device=device)
         gen.manual_seed(K * 7 + sum(Ns) + len(Ns) - 1)
         rng = np.random.default_rng(K + sum(Ns) + len(Ns) - 1)
         reps = max(2, int(ring_bytes // (K * sum(Ns) // 2)) + 1)
-        ring = [[gptq(K, N, act, gen) if fmt == "gptq" else exl2(K, N, gen, rng) for N in Ns] for _ in range(reps)]
+        ring = [[gptq(K, N, act, gen) if fmt == "gptq" else exl2(K, N, gen, rng, fmt == "exl2_qs") for N in Ns]
+                for _ in range(reps)]
 
         def call(i, x, ys, ws):
             if len(Ns) == 1:
@@ -432,7 +442,8 @@ def run_exq(args, rank, world, device):
 
     torch.cuda.set_device(device)
     grouped = not args.ungrouped
-    calls, x_all, y_all = build_stream(exq, torch, args.layers, device, grouped=grouped)
+    two_level = args.format == "exl2_qscale"
+    calls, x_all, y_all = build_stream(exq, torch, args.layers, device, grouped=grouped, two_level=two_level)
     per_layer = len(calls) // args.layers
     bytes_per_step = sum(w.packed_bytes for ws_, _, _ in calls for w in ws_)
     n_linears = sum(len(ws_) for ws_, _, _ in calls)
@@ -510,7 +521,7 @@ def run_exq(args, rank, world, device):
     e2e_gbs = job_throughput(bytes_per_step, args.steps, t_e2e_ms, world)
     peak, peak_kind = measured_peaks()
     per_gpu = gbs / world
-    traffic_ratio = profile_traffic()
+    traffic_ratio = None if two_level else profile_traffic()
     bytes_per_launch = bytes_per_step / n_launch
     result = {
         "metric": METRIC,
@@ -526,8 +537,9 @@ def run_exq(args, rank, world, device):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": "decode_stream_70b_exl2_4p0bpw",
+            "workload": "decode_stream_70b_exl2_4p0bpw" + ("_two_level_scales" if two_level else ""),
             "model_shape": "Llama-2-70B (80 layers x q,k,v,o,gate,up,down)",
+            "scales": "4-bit group-scale codes x fp16 column maxima" if two_level else "fp16 per (segment, column)",
             "layers": args.layers,
             "M": 1,
             "bpw": 4.0,
@@ -537,7 +549,7 @@ def run_exq(args, rank, world, device):
             "grouping": "q+k+v and gate+up share x: exq_gemv_multi" if grouped else "one exq_gemv per linear",
             "tokens_per_s": round(1000.0 / (t_ms / args.steps), 2),
             "pct_of_8TBps": round(100 * per_gpu / NOMINAL_HBM_GBS, 2),
-            "l2": "inputs larger than L2 (the packed stream is 38.5 GB per step)",
+            "l2": f"inputs larger than L2 (the packed stream is {bytes_per_step / 1e9:.1f} GB per step)",
             "launch": "one CUDA graph per step, programmatic dependent launch between GEMVs",
             "parallelism": f"replicas x{world}",
         },
@@ -550,7 +562,8 @@ def run_exq(args, rank, world, device):
             "frac": round(per_gpu / peak, 4),
             "traffic": None if traffic_ratio is None else round(traffic_ratio * bytes_per_launch),
             "algorithmic_bytes_per_launch": round(bytes_per_launch),
-            "kernel": "gemv_kernel<EXL2, M<=8> (+ gather_x_kernel per act-order call)",
+            "kernel": ("gemv_kernel<EXL2_QSCALE, M<=8>" if two_level else "gemv_kernel<EXL2, M<=8>")
+                      + " (+ gather_x_kernel per act-order call)",
         },
         "e2e": {
             "value": round(e2e_gbs, 2),

@@ -56,6 +56,16 @@ Readings where the pages are silent (each one is listed in the design doc):
   row j. Every group must hold exactly ``group_size`` rows.
 * The output is y = x . W accumulated in float64 here; the device path rounds
   its fp32 accumulator to fp16 once.
+* Quantized KV cache (Q4 / Q6 / Q8: the blog post's comparison table, "Step 2:
+  Use the right cache mode for your context length" and the VRAM estimate of
+  "Production Considerations", which give only the bytes per element). The
+  codec is not described; the reading here: a group is the D values of one
+  (token, head), symmetric with qmax = 2^(b-1) - 1,
+  s = fp16_RNE(fp32_RNE(amax / qmax)), q = clamp(rint(fp32_RNE(x / s)),
+  -qmax - 1, qmax) (q = 0 where s = 0), stored u = q + 2^(b-1) as a b-bit
+  code, code i at bits [i*b, i*b+b) of the group's little-endian word
+  stream, read back as fp16_RNE((u - 2^(b-1)) * s). The integer decisions are
+  taken in IEEE fp32 (numpy float32 division and rint), as on the device.
 """
 from __future__ import annotations
 
@@ -68,6 +78,7 @@ __all__ = [
     "exl2_seg_word_off", "pack_exl2", "unpack_exl2_codes", "dequant_exl2",
     "dequant_exl2_definitional", "pack_exl2_qscale", "unpack_exl2_qscale", "exl2_two_level_scales",
     "dequant_exl2_qscale", "matmul", "quantize_rtn", "EXL2_BITS", "SEGMENT_ROWS",
+    "KV_BITS", "kv_quantize", "kv_pack", "kv_unpack", "kv_dequantize",
 ]
 
 # ----------------------------------------------------------------------------
@@ -404,6 +415,66 @@ def dequant_exl2_qscale(qweight, seg_word_off, bits, q_scale, scale_max, perm, c
     N = q_scale.shape[1] * 8
     s = exl2_two_level_scales(unpack_exl2_qscale(q_scale, N), scale_max)
     return dequant_exl2(qweight, seg_word_off, bits, s, perm, cols=cols)
+
+
+# ----------------------------------------------------------------------------
+# Quantized KV cache codec (Q4 / Q6 / Q8)
+# ----------------------------------------------------------------------------
+
+KV_BITS = (4, 6, 8)
+
+
+def kv_quantize(x, b: int):
+    """fp16 x [G, D] (numpy float16 or uint16 bits) -> (codes uint8 [G, D],
+    scales uint16 fp16 bits [G]); the steps of the codec reading above."""
+    if b not in KV_BITS:
+        raise ValueError("b must be 4, 6 or 8")
+    x32 = _as_f64(x).astype(np.float32)                  # exact: fp16 values are fp32 values
+    qmax = (1 << (b - 1)) - 1
+    amax = np.abs(x32).max(axis=1)
+    s32 = amax / np.float32(qmax)                        # IEEE fp32 division, round to nearest even
+    s_bits = fp16_bits_from_float64(s32.astype(np.float64))
+    s = float64_from_fp16_bits(s_bits).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = x32 / s[:, None]                             # fp32 quotient
+    q = np.where(s[:, None] == 0, np.float32(0), np.rint(r))
+    q = np.clip(q, -qmax - 1, qmax).astype(np.int64)
+    return (q + (1 << (b - 1))).astype(np.uint8), s_bits
+
+
+def kv_pack(codes, b: int) -> np.ndarray:
+    """uint8 codes [G, D] -> uint32 [G, D*b/32]: code i of a group at bits
+    [i*b, i*b+b) of its word stream, one bit at a time."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    G, D = codes.shape
+    if (D * b) % 32:
+        raise ValueError("D * b must be a multiple of 32")
+    out = np.zeros((G, D * b // 32), dtype=np.uint32)
+    for i in range(D):
+        for t in range(b):
+            p = i * b + t
+            bit = ((codes[:, i] >> t) & 1).astype(np.uint32)
+            out[:, p // 32] |= bit << np.uint32(p % 32)
+    return out
+
+
+def kv_unpack(words, b: int, D: int) -> np.ndarray:
+    """uint32 [G, D*b/32] -> uint8 codes [G, D], one bit at a time."""
+    words = np.asarray(words, dtype=np.uint32)
+    out = np.zeros((words.shape[0], D), dtype=np.uint8)
+    for i in range(D):
+        for t in range(b):
+            p = i * b + t
+            bit = ((words[:, p // 32] >> np.uint32(p % 32)) & np.uint32(1)).astype(np.uint8)
+            out[:, i] |= bit << t
+    return out
+
+
+def kv_dequantize(words, scales, b: int, D: int) -> np.ndarray:
+    """fp16 bits [G, D] of fp16_RNE((u - 2^(b-1)) * s); the product is exact
+    in float64."""
+    u = kv_unpack(words, b, D).astype(np.int64) - (1 << (b - 1))
+    return fp16_bits_from_float64(u.astype(np.float64) * _as_f64(scales)[:, None])
 
 
 # ----------------------------------------------------------------------------

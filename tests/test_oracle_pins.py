@@ -483,3 +483,94 @@ def test_exl2_qscale_dequant_reduces_to_fp16_scales():
     assert np.array_equal(W_top, O.dequant_exl2_definitional(inp.q, inp.bits, np.tile(m, (8, 1)), inp.perm))
     cols = np.array([0, 9, 47])
     assert np.array_equal(O.dequant_exl2_qscale(qw, off, inp.bits, qs, m, perm, cols=cols), W[:, cols])
+
+
+# ---------------------------------------------------------------- quantized KV cache codec
+
+def _kv_golden():
+    rows = _fixture("kv_codec.txt")
+    x = np.array([int(t, 16) for t in rows[0].split()[1:]] + [0] * 24, dtype=np.uint16)
+    cases = []
+    for row in rows[1:]:
+        tok = row.split()
+        i_s, i_u, i_w, i_x = tok.index("s"), tok.index("u"), tok.index("words"), tok.index("xhat")
+        cases.append((int(tok[1]), int(tok[i_s + 1], 16), [int(t) for t in tok[i_u + 1:i_w]],
+                      [int(t, 16) for t in tok[i_w + 1:i_x]], [int(t, 16) for t in tok[i_x + 1:]]))
+    return x, cases
+
+
+def test_kv_codec_golden():
+    x, cases = _kv_golden()
+    for b, s_want, u_want, words_want, xhat_want in cases:
+        u, s = O.kv_quantize(x[None, :], b)
+        assert int(s[0]) == s_want, b
+        assert u[0, :8].tolist() == u_want, b
+        assert (u[0, 8:] == 1 << (b - 1)).all(), b
+        words = O.kv_pack(u, b)
+        assert [int(w) for w in words[0]] == words_want, b
+        assert np.array_equal(O.kv_unpack(words, b, 32), u)
+        xh = O.kv_dequantize(words, s, b, 32)
+        assert [int(v) for v in xh[0, :8]] == xhat_want, b
+
+
+def test_kv_codec_properties():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((300, 128)) * np.exp2(rng.integers(-12, 4, (300, 1)))).astype(np.float16)
+    x[0] = 0                                    # an all-zero group
+    x[1, :] = np.float16(-0.0)
+    x[2, 5] = np.float16(65504.0)               # the largest finite value
+    x[3, :] = np.float16(2.0 ** -24)            # amax / qmax rounds to a zero scale
+    x[4, :] = (rng.standard_normal(128) * 2.0 ** -17).astype(np.float16)  # a subnormal scale at every width
+    for b in O.KV_BITS:
+        qmax = (1 << (b - 1)) - 1
+        u, s = O.kv_quantize(x, b)
+        q = u.astype(np.int64) - (1 << (b - 1))
+        sv = O.float64_from_fp16_bits(s)
+        xv = O.float64_from_fp16_bits(x.view(np.uint16))
+        # with a normal fp16 scale (relative rounding <= 2^-11) the amax element
+        # takes the largest code; mirrored inputs mirror the codes
+        amax_i = np.abs(xv).argmax(axis=1)
+        big = sv > 0
+        normal = sv >= 2.0 ** -14
+        assert normal.sum() > 150 and (~normal & big).any()   # both kinds occur
+        assert (np.abs(q[np.arange(300), amax_i])[normal] == qmax).all(), b
+        u_neg, s_neg = O.kv_quantize(-x, b)
+        q_neg = u_neg.astype(np.int64) - (1 << (b - 1))
+        assert np.array_equal(s_neg, s) and np.array_equal(q_neg[normal], -q[normal]), b
+        # zero scales give zero codes and +0 outputs
+        assert (q[~big] == 0).all() and not big[0] and not big[3], b
+        xh = O.float64_from_fp16_bits(O.kv_dequantize(O.kv_pack(u, b), s, b, 128))
+        assert (xh[~big] == 0).all() and not np.signbit(xh[~big]).any()
+        # |x - xhat| <= s/2 (quotient and code rounding) + half an fp16 ulp of xhat
+        err = np.abs(xh - xv)
+        bound = 0.5 * sv[:, None] * (1 + 2.0 ** -20) + 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(xh), 2.0 ** -14))) - 10)
+        assert (err[normal] <= bound[normal]).all(), b
+        # a subnormal scale may clamp the largest codes: the error is then bounded by amax
+        assert (err[big & ~normal] <= 2 * np.abs(xv).max(axis=1, keepdims=True)[big & ~normal]).all(), b
+        # monotone codes within a group
+        order = np.argsort(xv, axis=1, kind="stable")
+        assert (np.diff(np.take_along_axis(q, order, axis=1), axis=1) >= 0).all(), b
+
+
+def test_kv_stream_layout_is_the_exl2_column_stream():
+    # a 32-value group packs exactly as one EXL2 segment column of the same width,
+    # built by the other packer and by a Python big integer
+    rng = np.random.default_rng(4)
+    for b in O.KV_BITS:
+        u = rng.integers(0, 1 << b, size=(3, 32)).astype(np.uint8)
+        words = O.kv_pack(u, b)
+        qw, _, _, _ = O.pack_exl2(u.T.copy(), [b], np.ones((1, 3), np.float16), None)
+        assert np.array_equal(words, qw.T), b
+        stream = sum(int(v) << (i * b) for i, v in enumerate(u[1]))
+        assert [int(w) for w in words[1]] == [(stream >> (32 * t)) & 0xFFFFFFFF for t in range(b)], b
+
+
+def test_kv_codec_ties_round_to_even():
+    # s = fp16(1/7) = 1170 x 2^-13; x = 585 x 2^-13 and 1755 x 2^-13 are fp16
+    # values whose quotients are exactly 0.5 and 1.5 in fp32: ties go to the
+    # even code (0 and 2), also for the negative tie
+    x = np.zeros((1, 32), np.float64)
+    x[0, :4] = [1.0, 585 * 2.0 ** -13, -585 * 2.0 ** -13, 1755 * 2.0 ** -13]
+    u, s = O.kv_quantize(x.astype(np.float16), 4)
+    assert int(s[0]) == 0x3092
+    assert (u[0, :4].astype(int) - 8).tolist() == [7, 0, 0, 2]

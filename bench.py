@@ -68,6 +68,9 @@ def parse_args():
                          "the linears that share x (q/k/v, gate/up) into exq_gemv_multi calls")
     ap.add_argument("--prefill", action="store_true",
                     help="time the prefill GEMM over the 70B shapes instead (one JSON line, TFLOPS per shape)")
+    ap.add_argument("--kv", action="store_true",
+                    help="time the quantized KV cache codec (Q4/Q6/Q8 write and read) over a Llama-2-70B cache "
+                         "at 32K context instead (one JSON line, GB/s per width and direction)")
     ap.add_argument("--decode-sweep", action="store_true",
                     help="time single GEMVs of the GPTQ 4096, GPTQ act-order 7B and EXL2 4.0 7B workloads "
                          "instead (one JSON line, GB/s per shape and M)")
@@ -415,6 +418,79 @@ def run_decode_sweep(args, device):
     }
 
 
+def run_kv(args, device):
+    """The quantized KV cache codec over a Llama-2-70B cache at 32K context:
+    80 layers x K and V x 32768 tokens x 8 KV heads = 41,943,040 groups of
+    D = 128 fp16 values (10.7 GB), values N(0, 1) times a per-group power of
+    two in 2^-6 .. 2^2. For each width, `--steps` quantize launches and
+    `--steps` dequantize launches after `--warmup`, CUDA events around each
+    run; GB/s = bytes read + written per launch / time (far above L2)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    peak, peak_kind = measured_peaks()
+    G, D = 80 * 2 * 32768 * 8, 128
+    gen = torch.Generator(device=device)
+    gen.manual_seed(11)
+    x = torch.empty(G, D, dtype=torch.float16, device=device)
+    chunk = 1 << 22
+    for i in range(0, G, chunk):  # drawn in slices to bound the fp32 temporaries
+        n = min(chunk, G - i)
+        x[i:i + n] = (torch.randn(n, D, device=device, generator=gen) *
+                      torch.exp2(torch.randint(-6, 3, (n, 1), device=device, generator=gen).float())).half()
+    out = torch.empty_like(x)
+    widths = {}
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000 / args.steps  # us
+
+    for bits in (4, 6, 8):
+        codes = torch.empty(G, D * bits // 32, dtype=torch.int32, device=device)
+        scales = torch.empty(G, dtype=torch.float16, device=device)
+        q_us = timed(lambda: exq.exq_kv_quantize(x, bits, codes, scales))
+        d_us = timed(lambda: exq.exq_kv_dequantize(codes, scales, D, bits, out))
+        packed = G * D * bits // 8 + 2 * G
+        q_gbs = (2 * G * D + packed) / q_us / 1e3
+        d_gbs = (packed + 2 * G * D) / d_us / 1e3
+        widths[f"Q{bits}"] = {
+            "quantize_us": round(q_us, 1), "quantize_GB/s": round(q_gbs, 1), "quantize_frac": round(q_gbs / peak, 4),
+            "dequantize_us": round(d_us, 1), "dequantize_GB/s": round(d_gbs, 1),
+            "dequantize_frac": round(d_gbs / peak, 4),
+            "cache_bytes": packed, "fp16_bytes": 2 * G * D,
+        }
+        del codes, scales
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the KV codec run")
+    return {
+        "metric": "quantized KV cache codec GB/s (bytes read + written per pass)",
+        "value": min(min(v["quantize_GB/s"], v["dequantize_GB/s"]) for v in widths.values()),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "kv_cache_70b_32k", "groups": G, "D": D, "value_is": "slowest width and direction",
+                   "l2": "inputs larger than L2 (10.7 GB of fp16 per pass)"},
+        "roofline": {"bound": "hbm", "peak": peak, "unit": UNIT, "peak_kind": peak_kind},
+        "widths": widths,
+    }
+
+
 def max_over_ranks(times, world, device=None):
     """The slowest rank's times: every rank waits for all of them (all-reduce
     MAX over the process group; a CPU tensor under gloo)."""
@@ -669,6 +745,10 @@ def main():
     if args.prefill:
         if rank == 0:
             print(json.dumps(run_prefill(args, torch.device("cuda", local))), flush=True)
+        return
+    if args.kv:
+        if rank == 0:
+            print(json.dumps(run_kv(args, torch.device("cuda", local))), flush=True)
         return
     if args.decode_sweep:
         if rank == 0:

@@ -267,6 +267,36 @@ exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t*
 #define EXQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 exq_status exq_gemm_noalloc(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* stream);
 
+/* ---------------------------------------------------------------- quantized KV cache */
+
+/* Quantized KV cache codec, Q4 / Q6 / Q8 (ExLlamaV2 blog post: comparison
+ * table and "Step 2: Use the right cache mode for your context length" name
+ * the Q4 / Q6 / Q8 cache; "Production Considerations" costs it at half a byte
+ * and one byte per element for Q4 / Q8). The pages do not describe the codec;
+ * this one quantises groups of D values (one token's one head of K or V),
+ * symmetric, qmax = 2^(bits-1) - 1:
+ *   s = fp16_RNE(fp32_RNE(amax / qmax)),
+ *   q = clamp(rint(fp32_RNE(x / s)), -qmax - 1, qmax)   (q = 0 where s = 0),
+ *   stored code u = q + 2^(bits-1); code i of a group at bits
+ *   [i*bits, i*bits + bits) of the group's little-endian uint32 stream;
+ *   read back as fp16_RNE((u - 2^(bits-1)) * s).
+ * rint rounds half to even. Inputs must be finite.
+ *   x       device fp16 [n_groups, D]
+ *   codes   device uint32 [n_groups, D * bits / 32]
+ *   scales  device fp16 [n_groups]
+ * D must be 64, 128 or 256 and bits 4, 6 or 8, else EXQ_ERR_UNSUPPORTED;
+ * n_groups < 0, a NULL or misaligned pointer (16 bytes) is EXQ_ERR_INVALID_ARG;
+ * n_groups = 0 launches nothing and returns EXQ_OK (the pointers are then not
+ * looked at and may be NULL). Outputs are fully overwritten; the same
+ * inputs give the same bits. */
+exq_status exq_kv_quantize(const uint16_t* x, int64_t n_groups, int32_t D, int32_t bits, uint32_t* codes,
+                           uint16_t* scales, void* stream);
+
+/* exq_kv_dequantize -- the inverse read: x_out fp16 [n_groups, D] from codes
+ * and scales as written by exq_kv_quantize (same argument rules). */
+exq_status exq_kv_dequantize(const uint32_t* codes, const uint16_t* scales, int64_t n_groups, int32_t D,
+                             int32_t bits, uint16_t* x_out, void* stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Static, NUL-terminated description of a status code. */

@@ -173,6 +173,36 @@ extern "C" exq_status exq_gemm_noalloc(const exq_weight* w, const uint16_t* x, i
   return launch_gemm_noalloc(*w, x, M, y, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// EXQ_OK with `empty` set: nothing to do (n_groups == 0; the pointers are not used)
+exq_status check_kv(const void* a, const void* b, const void* c, long long n_groups, int D, int bits, bool& empty) {
+  if (n_groups < 0) return EXQ_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128 && D != 256) || (bits != 4 && bits != 6 && bits != 8)) return EXQ_ERR_UNSUPPORTED;
+  empty = n_groups == 0;
+  if (empty) return EXQ_OK;
+  if (!a || !b || !c || !aligned16(a) || !aligned16(b) || !aligned16(c)) return EXQ_ERR_INVALID_ARG;
+  return EXQ_OK;
+}
+}  // namespace
+
+extern "C" exq_status exq_kv_quantize(const uint16_t* x, int64_t n_groups, int32_t D, int32_t bits, uint32_t* codes,
+                                      uint16_t* scales, void* stream) {
+  bool empty = false;
+  const exq_status st = check_kv(x, codes, scales, n_groups, D, bits, empty);
+  if (st != EXQ_OK || empty) return st;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_kv_quantize(x, n_groups, D, bits, codes, scales, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" exq_status exq_kv_dequantize(const uint32_t* codes, const uint16_t* scales, int64_t n_groups, int32_t D,
+                                        int32_t bits, uint16_t* x_out, void* stream) {
+  bool empty = false;
+  const exq_status st = check_kv(codes, scales, x_out, n_groups, D, bits, empty);
+  if (st != EXQ_OK || empty) return st;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_kv_dequantize(codes, scales, n_groups, D, bits, x_out, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" const char* exq_status_string(exq_status s) {
   switch (s) {
     case EXQ_OK: return "ok";

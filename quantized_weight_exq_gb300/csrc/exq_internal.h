@@ -50,6 +50,12 @@ size_t gemm_gather_bytes(const exq_weight& w, int M);
 // exq_gemm with the library's static scratch array as the workspace
 exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream);
 
+// quantized KV cache codec (D in {64, 128, 256}, b in {4, 6, 8}, checked by the caller)
+exq_status launch_kv_quantize(const uint16_t* x, long long n_groups, int D, int b, uint32_t* codes,
+                              uint16_t* scales, cudaStream_t stream);
+exq_status launch_kv_dequantize(const uint32_t* codes, const uint16_t* scales, long long n_groups, int D, int b,
+                                uint16_t* x_out, cudaStream_t stream);
+
 // read-and-clear of each module's device error word (stream-ordered copy +
 // synchronise); returns the OR of the codes or ~0u on a CUDA failure
 unsigned take_gemv_errors(cudaStream_t stream);

@@ -1,0 +1,169 @@
+// Quantized KV cache codec, Q4 / Q6 / Q8.
+//
+// The ExLlamaV2 blog post ("ExLlamaV2: The fastest inference engine for
+// quantized Llama/HF models") lists a Q4 / Q6 / Q8 KV cache (comparison table;
+// "Step 2: Use the right cache mode for your context length") and costs it
+// at half a byte (Q4) and one byte (Q8) per cached element ("Production
+// Considerations", VRAM estimate); the codec itself is not described. This
+// one: a group is the D values of one (token, head); symmetric with
+// qmax = 2^(b-1) - 1;
+//   s = fp16_RN(fp32_RN(amax / qmax)),
+//   q = clamp(rint(fp32_RN(x / s)), -qmax - 1, qmax)  (0 where s = 0),
+//   u = q + 2^(b-1), code i of the group at bits [i b, i b + b) of its
+//   little-endian word stream;
+// read back as fp16_RN((u - 2^(b-1)) s). Every integer decision is an IEEE
+// fp32 division rounded to nearest even, then round-half-even to an integer.
+//
+// Both kernels are bound by HBM: one warp per group, lane l holding the D / 32
+// consecutive values [l D/32, (l+1) D/32), so each group moves as one
+// contiguous block (D * 2 bytes of fp16, D * b / 8 bytes of codes).
+#include "exq_device.cuh"
+#include "exq_internal.h"
+
+namespace exq {
+namespace {
+
+constexpr int kWarps = 8;  // groups per 256-thread block
+
+template <int VPL>  // values per lane: D / 32
+struct Vec;
+template <>
+struct Vec<2> {
+  using T = uint32_t;
+};
+template <>
+struct Vec<4> {
+  using T = uint2;
+};
+template <>
+struct Vec<8> {
+  using T = uint4;
+};
+
+template <int VPL>
+__device__ __forceinline__ void unpack_halves(const typename Vec<VPL>::T& v, uint32_t (&h)[VPL]) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+  for (int i = 0; i < VPL / 2; ++i) {
+    h[2 * i] = w[i] & 0xFFFFu;
+    h[2 * i + 1] = w[i] >> 16;
+  }
+}
+
+template <int VPL, int B>
+__global__ void __launch_bounds__(kWarps * 32)
+    kv_quantize_kernel(const uint16_t* __restrict__ x, long long n_groups, uint32_t* __restrict__ codes,
+                       uint16_t* __restrict__ scales) {
+  constexpr int D = 32 * VPL;
+  constexpr int kWords = D * B / 32;   // words of a group
+  constexpr int kChunk = VPL * B;      // bits of one lane (8..64)
+  constexpr int kQmax = (1 << (B - 1)) - 1;
+  __shared__ uint32_t words[kWarps][kWords];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long g = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  if (g >= n_groups) return;  // warp-uniform
+
+  using V = typename Vec<VPL>::T;
+  const V raw = *reinterpret_cast<const V*>(x + g * D + lane * VPL);
+  uint32_t h[VPL];
+  unpack_halves<VPL>(raw, h);
+  float xf[VPL];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    xf[i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i])));
+    amax = fmaxf(amax, fabsf(xf[i]));
+  }
+  // non-negative floats order as their bit patterns
+  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+  const __half s16 = __float2half_rn(__fdiv_rn(amax, static_cast<float>(kQmax)));
+  const float s = __half2float(s16);
+
+  unsigned long long chunk = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int q = 0;
+    if (s != 0.f) q = max(-kQmax - 1, min(kQmax, __float2int_rn(__fdiv_rn(xf[i], s))));
+    chunk |= static_cast<unsigned long long>(q + (1 << (B - 1))) << (i * B);
+  }
+
+  // the lane's bits sit at stream offset lane * kChunk and touch at most two words
+  for (int i = lane; i < kWords; i += 32) words[warp][i] = 0u;
+  __syncwarp();
+  const int off = lane * kChunk;
+  const unsigned long long win = chunk << (off & 31);
+  atomicOr(&words[warp][off >> 5], static_cast<uint32_t>(win));
+  if ((off & 31) + kChunk > 32) atomicOr(&words[warp][(off >> 5) + 1], static_cast<uint32_t>(win >> 32));
+  __syncwarp();
+  for (int i = lane; i < kWords; i += 32) codes[g * kWords + i] = words[warp][i];
+  if (lane == 0) scales[g] = __half_as_ushort(s16);
+}
+
+template <int VPL, int B>
+__global__ void __launch_bounds__(kWarps * 32)
+    kv_dequantize_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales, long long n_groups,
+                         uint16_t* __restrict__ x_out) {
+  constexpr int D = 32 * VPL;
+  constexpr int kWords = D * B / 32;
+  constexpr int kChunk = VPL * B;
+  constexpr uint32_t kMask = (1u << B) - 1u;
+  constexpr int kZ = 1 << (B - 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long g = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  if (g >= n_groups) return;
+
+  const int off = lane * kChunk;
+  const uint32_t* gw = codes + g * kWords;
+  const uint32_t lo = __ldg(gw + (off >> 5));
+  const uint32_t hi = (off & 31) + kChunk > 32 ? __ldg(gw + (off >> 5) + 1) : 0u;  // inside the group
+  const unsigned long long win = ((static_cast<unsigned long long>(hi) << 32) | lo) >> (off & 31);
+  const uint32_t s = __ldg(scales + g);
+  const uint32_t s2 = s | (s << 16);
+  // (u - z) exactly in fp16: u planted in the mantissa of 1024, then - (1024 + z)
+  constexpr uint32_t bias = pack2(f16_bits(-(1024 + kZ)), f16_bits(-(1024 + kZ)));
+  uint32_t out[VPL / 2];
+#pragma unroll
+  for (int i = 0; i < VPL / 2; ++i) {
+    const uint32_t u0 = static_cast<uint32_t>(win >> (2 * i * B)) & kMask;
+    const uint32_t u1 = static_cast<uint32_t>(win >> ((2 * i + 1) * B)) & kMask;
+    out[i] = hmul2(hadd2(u0 | (u1 << 16) | kMagic, bias), s2);
+  }
+  using V = typename Vec<VPL>::T;
+  *reinterpret_cast<V*>(x_out + g * D + lane * VPL) = *reinterpret_cast<const V*>(out);
+}
+
+using QuantFn = void (*)(const uint16_t*, long long, uint32_t*, uint16_t*);
+using DequantFn = void (*)(const uint32_t*, const uint16_t*, long long, uint16_t*);
+
+template <int VPL>
+QuantFn quant_for_bits(int b) {
+  return b == 4 ? kv_quantize_kernel<VPL, 4> : b == 6 ? kv_quantize_kernel<VPL, 6> : kv_quantize_kernel<VPL, 8>;
+}
+template <int VPL>
+DequantFn dequant_for_bits(int b) {
+  return b == 4 ? kv_dequantize_kernel<VPL, 4>
+                : b == 6 ? kv_dequantize_kernel<VPL, 6> : kv_dequantize_kernel<VPL, 8>;
+}
+
+dim3 grid_for(long long n_groups) { return dim3(static_cast<unsigned>((n_groups + kWarps - 1) / kWarps)); }
+
+}  // namespace
+
+exq_status launch_kv_quantize(const uint16_t* x, long long n_groups, int D, int b, uint32_t* codes,
+                              uint16_t* scales, cudaStream_t stream) {
+  if (n_groups == 0) return EXQ_OK;
+  const QuantFn fn = D == 64 ? quant_for_bits<2>(b) : D == 128 ? quant_for_bits<4>(b) : quant_for_bits<8>(b);
+  fn<<<grid_for(n_groups), kWarps * 32, 0, stream>>>(x, n_groups, codes, scales);
+  return cudaGetLastError() == cudaSuccess ? EXQ_OK : EXQ_ERR_CUDA;
+}
+
+exq_status launch_kv_dequantize(const uint32_t* codes, const uint16_t* scales, long long n_groups, int D, int b,
+                                uint16_t* x_out, cudaStream_t stream) {
+  if (n_groups == 0) return EXQ_OK;
+  const DequantFn fn =
+      D == 64 ? dequant_for_bits<2>(b) : D == 128 ? dequant_for_bits<4>(b) : dequant_for_bits<8>(b);
+  fn<<<grid_for(n_groups), kWarps * 32, 0, stream>>>(codes, scales, n_groups, x_out);
+  return cudaGetLastError() == cudaSuccess ? EXQ_OK : EXQ_ERR_CUDA;
+}
+
+}  // namespace exq

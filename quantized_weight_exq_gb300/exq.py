@@ -31,7 +31,7 @@ EXQ_FMT_EXL2_QSCALE = 3
 EXPORTED = (
     "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
     "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
-    "exq_get_last_device_error",
+    "exq_get_last_device_error", "exq_kv_quantize", "exq_kv_dequantize",
 )
 
 # most layers one exq_gemv_multi call takes (EXQ_GEMV_MAX_LAYERS)
@@ -77,6 +77,8 @@ def _load():
         "exq_gemm_workspace_size": (sz, [W, i32]),
         "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
         "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
+        "exq_kv_quantize": (st, [P, i64, i32, i32, P, P, P]),
+        "exq_kv_dequantize": (st, [P, P, i64, i32, i32, P, P]),
         "exq_status_string": (ctypes.c_char_p, [st]),
         "exq_get_last_device_error": (st, [P]),
     }
@@ -321,6 +323,32 @@ def exq_gemm_noalloc(w: Weight, x, y, stream=None):
     _check(_lib.exq_gemm_noalloc(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(),
                                  _stream_ptr(stream)), "exq_gemm_noalloc")
     return y
+
+
+def exq_kv_quantize(x, bits: int, codes=None, scales=None, stream=None):
+    """Quantized KV cache write: x fp16 [..., D] (groups of D values) ->
+    (codes int32 [groups, D * bits / 32] holding uint32 words, scales fp16 [groups])."""
+    import torch
+    D = x.shape[-1]
+    G = x.numel() // D if D else 0
+    if codes is None:
+        codes = torch.empty(G, D * bits // 32, dtype=torch.int32, device=x.device)
+    if scales is None:
+        scales = torch.empty(G, dtype=torch.float16, device=x.device)
+    _check(_lib.exq_kv_quantize(x.data_ptr(), G, D, bits, codes.data_ptr(), scales.data_ptr(), _stream_ptr(stream)),
+           "exq_kv_quantize")
+    return codes, scales
+
+
+def exq_kv_dequantize(codes, scales, D: int, bits: int, out=None, stream=None):
+    """Quantized KV cache read: fp16 [groups, D]."""
+    import torch
+    G = scales.numel()
+    if out is None:
+        out = torch.empty(G, D, dtype=torch.float16, device=scales.device)
+    _check(_lib.exq_kv_dequantize(codes.data_ptr(), scales.data_ptr(), G, D, bits, out.data_ptr(),
+                                  _stream_ptr(stream)), "exq_kv_dequantize")
+    return out
 
 
 def exq_get_last_device_error(stream=None) -> int:

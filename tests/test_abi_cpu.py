@@ -190,3 +190,28 @@ def test_two_level_descriptor_rules(exq):
     arr = (exq.exq_weight * 2)(_desc(exq, **qs), e)
     yp = (ctypes.c_void_p * 2)(0x60000, 0x61000)
     assert lib.exq_gemv_multi(arr, 2, 0x50000, 1, yp, None, 0, None) == exq.EXQ_ERR_INVALID_ARG
+
+
+def test_kv_codec_validates_on_host(exq):
+    from quantized_weight_exq_gb300 import exq as mod
+    lib = mod._lib
+    ok = dict(a=0x50000, G=4, D=128, bits=4, b=0x60000, c=0x70000)
+
+    def q(**kw):
+        d = {**ok, **kw}
+        return lib.exq_kv_quantize(d["a"], d["G"], d["D"], d["bits"], d["b"], d["c"], None)
+
+    def dq(**kw):
+        d = {**ok, **kw}
+        return lib.exq_kv_dequantize(d["a"], d["b"], d["G"], d["D"], d["bits"], d["c"], None)
+
+    for f in (q, dq):
+        assert f(D=96) == exq.EXQ_ERR_UNSUPPORTED
+        assert f(D=512) == exq.EXQ_ERR_UNSUPPORTED
+        assert f(bits=5) == exq.EXQ_ERR_UNSUPPORTED
+        assert f(bits=2) == exq.EXQ_ERR_UNSUPPORTED
+        assert f(G=-1) == exq.EXQ_ERR_INVALID_ARG
+        assert f(a=None) == exq.EXQ_ERR_INVALID_ARG
+        assert f(b=0x60008) == exq.EXQ_ERR_INVALID_ARG
+        assert f(c=None) == exq.EXQ_ERR_INVALID_ARG
+        assert f(G=0, a=None, b=None, c=None) == exq.EXQ_OK   # nothing to do, no launch

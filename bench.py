@@ -71,6 +71,8 @@ def parse_args():
     ap.add_argument("--kv", action="store_true",
                     help="time the quantized KV cache codec (Q4/Q6/Q8 write and read) over a Llama-2-70B cache "
                          "at 32K context instead (one JSON line, GB/s per width and direction)")
+    ap.add_argument("--kv-groups", type=int, default=80 * 2 * 32768 * 8,
+                    help="groups of 128 values for --kv (default: the whole 70B cache at 32K context)")
     ap.add_argument("--decode-sweep", action="store_true",
                     help="time single GEMVs of the GPTQ 4096, GPTQ act-order 7B and EXL2 4.0 7B workloads "
                          "instead (one JSON line, GB/s per shape and M)")
@@ -433,7 +435,7 @@ def run_kv(args, device):
 
     torch.cuda.set_device(device)
     peak, peak_kind = measured_peaks()
-    G, D = 80 * 2 * 32768 * 8, 128
+    G, D = args.kv_groups, 128
     gen = torch.Generator(device=device)
     gen.manual_seed(11)
     x = torch.empty(G, D, dtype=torch.float16, device=device)
@@ -484,8 +486,9 @@ def run_kv(args, device):
         "higher_is_better": True,
         "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": "kv_cache_70b_32k", "groups": G, "D": D, "value_is": "slowest width and direction",
-                   "l2": "inputs larger than L2 (10.7 GB of fp16 per pass)"},
+        "config": {"workload": "kv_cache_70b_32k" if G == 80 * 2 * 32768 * 8 else f"kv_cache_{G}_groups",
+                   "groups": G, "D": D, "value_is": "slowest width and direction",
+                   "l2": f"inputs larger than L2 ({2 * G * D / 1e9:.1f} GB of fp16 per pass)"},
         "roofline": {"bound": "hbm", "peak": peak, "unit": UNIT, "peak_kind": peak_kind},
         "widths": widths,
     }

@@ -14,9 +14,11 @@
 // read back as fp16_RN((u - 2^(b-1)) s). Every integer decision is an IEEE
 // fp32 division rounded to nearest even, then round-half-even to an integer.
 //
-// Both kernels are bound by HBM: one warp per group, lane l holding the D / 32
-// consecutive values [l D/32, (l+1) D/32), so each group moves as one
-// contiguous block (D * 2 bytes of fp16, D * b / 8 bytes of codes).
+// Both kernels are bound by HBM. A warp handles four groups, lane l holding
+// the D / 32 consecutive values [l D/32, (l+1) D/32) of each, so a group moves
+// as one contiguous block (D * 2 bytes of fp16, D * b / 8 bytes of codes); all
+// of a warp's loads are issued before any of its arithmetic, to keep enough
+// bytes in flight per SM.
 #include "exq_device.cuh"
 #include "exq_internal.h"
 
@@ -50,7 +52,18 @@ __device__ __forceinline__ void unpack_halves(const typename Vec<VPL>::T& v, uin
   }
 }
 
-template <int VPL, int B>
+// x / s rounded to an integer as rint(fp32_RN(x / s)): the quotient comes
+// from a multiply by fp32_RN(1 / s), which is within 3 * 2^-24 |x / s| of the
+// correctly rounded one; only where that leaves the quotient within 2^-14 of
+// a half-integer (|x / s| <= 256: 4.6e-5 < 2^-14) does the exact division
+// decide. Beyond 256 the code is clamped whichever quotient is used.
+__device__ __forceinline__ int round_quotient(float x, float s, float inv) {
+  float r = x * inv;
+  if (fabsf(fabsf(r - rintf(r)) - 0.5f) < 0x1p-14f) r = __fdiv_rn(x, s);
+  return __float2int_rn(r);
+}
+
+template <int VPL, int B, int GPW>
 __global__ void __launch_bounds__(kWarps * 32)
     kv_quantize_kernel(const uint16_t* __restrict__ x, long long n_groups, uint32_t* __restrict__ codes,
                        uint16_t* __restrict__ scales) {
@@ -58,48 +71,66 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int kWords = D * B / 32;   // words of a group
   constexpr int kChunk = VPL * B;      // bits of one lane (8..64)
   constexpr int kQmax = (1 << (B - 1)) - 1;
-  __shared__ uint32_t words[kWarps][kWords];
+  __shared__ uint32_t words[kWarps][GPW][kWords];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long g = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  if (g >= n_groups) return;  // warp-uniform
+  // the block's groups: k * kWarps + warp, k < GPW (each k a contiguous run of kWarps groups)
+  const long long g0 = static_cast<long long>(blockIdx.x) * kWarps * GPW + warp;
 
   using V = typename Vec<VPL>::T;
-  const V raw = *reinterpret_cast<const V*>(x + g * D + lane * VPL);
-  uint32_t h[VPL];
-  unpack_halves<VPL>(raw, h);
-  float xf[VPL];
-  float amax = 0.f;
+  V raw[GPW];
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    xf[i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i])));
-    amax = fmaxf(amax, fabsf(xf[i]));
+  for (int k = 0; k < GPW; ++k) {  // every load of the warp first
+    const long long g = g0 + k * kWarps;
+    if (g < n_groups) raw[k] = *reinterpret_cast<const V*>(x + g * D + lane * VPL);
   }
-  // non-negative floats order as their bit patterns
-  amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
-  const __half s16 = __float2half_rn(__fdiv_rn(amax, static_cast<float>(kQmax)));
-  const float s = __half2float(s16);
-
-  unsigned long long chunk = 0;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    int q = 0;
-    if (s != 0.f) q = max(-kQmax - 1, min(kQmax, __float2int_rn(__fdiv_rn(xf[i], s))));
-    chunk |= static_cast<unsigned long long>(q + (1 << (B - 1))) << (i * B);
-  }
+  for (int k = 0; k < GPW; ++k)
+    for (int i = lane; i < kWords; i += 32) words[warp][k][i] = 0u;
+  __syncwarp();
 
-  // the lane's bits sit at stream offset lane * kChunk and touch at most two words
-  for (int i = lane; i < kWords; i += 32) words[warp][i] = 0u;
+#pragma unroll
+  for (int k = 0; k < GPW; ++k) {
+    const long long g = g0 + k * kWarps;
+    if (g >= n_groups) break;  // warp-uniform
+    uint32_t h[VPL];
+    unpack_halves<VPL>(raw[k], h);
+    float xf[VPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      xf[i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h[i])));
+      amax = fmaxf(amax, fabsf(xf[i]));
+    }
+    // non-negative floats order as their bit patterns
+    amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
+    const __half s16 = __float2half_rn(__fdiv_rn(amax, static_cast<float>(kQmax)));
+    const float s = __half2float(s16);
+    const float inv = s != 0.f ? __frcp_rn(s) : 0.f;
+
+    unsigned long long chunk = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      int q = 0;
+      if (s != 0.f) q = max(-kQmax - 1, min(kQmax, round_quotient(xf[i], s, inv)));
+      chunk |= static_cast<unsigned long long>(q + (1 << (B - 1))) << (i * B);
+    }
+    // the lane's bits sit at stream offset lane * kChunk and touch at most two words
+    const int off = lane * kChunk;
+    const unsigned long long win = chunk << (off & 31);
+    atomicOr(&words[warp][k][off >> 5], static_cast<uint32_t>(win));
+    if ((off & 31) + kChunk > 32) atomicOr(&words[warp][k][(off >> 5) + 1], static_cast<uint32_t>(win >> 32));
+    if (lane == 0) scales[g] = __half_as_ushort(s16);
+  }
   __syncwarp();
-  const int off = lane * kChunk;
-  const unsigned long long win = chunk << (off & 31);
-  atomicOr(&words[warp][off >> 5], static_cast<uint32_t>(win));
-  if ((off & 31) + kChunk > 32) atomicOr(&words[warp][(off >> 5) + 1], static_cast<uint32_t>(win >> 32));
-  __syncwarp();
-  for (int i = lane; i < kWords; i += 32) codes[g * kWords + i] = words[warp][i];
-  if (lane == 0) scales[g] = __half_as_ushort(s16);
+#pragma unroll
+  for (int k = 0; k < GPW; ++k) {
+    const long long g = g0 + k * kWarps;
+    if (g >= n_groups) break;
+    for (int i = lane; i < kWords; i += 32) codes[g * kWords + i] = words[warp][k][i];
+  }
 }
 
-template <int VPL, int B>
+template <int VPL, int B, int GPW>
 __global__ void __launch_bounds__(kWarps * 32)
     kv_dequantize_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales, long long n_groups,
                          uint16_t* __restrict__ x_out) {
@@ -109,43 +140,61 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr uint32_t kMask = (1u << B) - 1u;
   constexpr int kZ = 1 << (B - 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long g = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  if (g >= n_groups) return;
-
+  const long long g0 = static_cast<long long>(blockIdx.x) * kWarps * GPW + warp;
   const int off = lane * kChunk;
-  const uint32_t* gw = codes + g * kWords;
-  const uint32_t lo = __ldg(gw + (off >> 5));
-  const uint32_t hi = (off & 31) + kChunk > 32 ? __ldg(gw + (off >> 5) + 1) : 0u;  // inside the group
-  const unsigned long long win = ((static_cast<unsigned long long>(hi) << 32) | lo) >> (off & 31);
-  const uint32_t s = __ldg(scales + g);
-  const uint32_t s2 = s | (s << 16);
+  constexpr bool kTwo = (kChunk & 31) != 0 || kChunk > 32;  // some lane's bits cross a word boundary
+
+  uint32_t lo[GPW], hi[GPW], sc[GPW];
+#pragma unroll
+  for (int k = 0; k < GPW; ++k) {  // every load of the warp first
+    const long long g = g0 + k * kWarps;
+    lo[k] = hi[k] = sc[k] = 0u;
+    if (g < n_groups) {
+      const uint32_t* gw = codes + g * kWords;
+      lo[k] = __ldg(gw + (off >> 5));
+      if (kTwo && (off & 31) + kChunk > 32) hi[k] = __ldg(gw + (off >> 5) + 1);  // inside the group
+      sc[k] = __ldg(scales + g);
+    }
+  }
   // (u - z) exactly in fp16: u planted in the mantissa of 1024, then - (1024 + z)
   constexpr uint32_t bias = pack2(f16_bits(-(1024 + kZ)), f16_bits(-(1024 + kZ)));
-  uint32_t out[VPL / 2];
 #pragma unroll
-  for (int i = 0; i < VPL / 2; ++i) {
-    const uint32_t u0 = static_cast<uint32_t>(win >> (2 * i * B)) & kMask;
-    const uint32_t u1 = static_cast<uint32_t>(win >> ((2 * i + 1) * B)) & kMask;
-    out[i] = hmul2(hadd2(u0 | (u1 << 16) | kMagic, bias), s2);
+  for (int k = 0; k < GPW; ++k) {
+    const long long g = g0 + k * kWarps;
+    if (g >= n_groups) break;
+    const unsigned long long win = ((static_cast<unsigned long long>(hi[k]) << 32) | lo[k]) >> (off & 31);
+    const uint32_t s2 = sc[k] | (sc[k] << 16);
+    uint32_t out[VPL / 2];
+#pragma unroll
+    for (int i = 0; i < VPL / 2; ++i) {
+      const uint32_t u0 = static_cast<uint32_t>(win >> (2 * i * B)) & kMask;
+      const uint32_t u1 = static_cast<uint32_t>(win >> ((2 * i + 1) * B)) & kMask;
+      out[i] = hmul2(hadd2(u0 | (u1 << 16) | kMagic, bias), s2);
+    }
+    using V = typename Vec<VPL>::T;
+    *reinterpret_cast<V*>(x_out + g * D + lane * VPL) = *reinterpret_cast<const V*>(out);
   }
-  using V = typename Vec<VPL>::T;
-  *reinterpret_cast<V*>(x_out + g * D + lane * VPL) = *reinterpret_cast<const V*>(out);
 }
+
+constexpr int kGpw = 4;  // groups per warp
 
 using QuantFn = void (*)(const uint16_t*, long long, uint32_t*, uint16_t*);
 using DequantFn = void (*)(const uint32_t*, const uint16_t*, long long, uint16_t*);
 
 template <int VPL>
 QuantFn quant_for_bits(int b) {
-  return b == 4 ? kv_quantize_kernel<VPL, 4> : b == 6 ? kv_quantize_kernel<VPL, 6> : kv_quantize_kernel<VPL, 8>;
+  return b == 4 ? kv_quantize_kernel<VPL, 4, kGpw>
+                : b == 6 ? kv_quantize_kernel<VPL, 6, kGpw> : kv_quantize_kernel<VPL, 8, kGpw>;
 }
 template <int VPL>
 DequantFn dequant_for_bits(int b) {
-  return b == 4 ? kv_dequantize_kernel<VPL, 4>
-                : b == 6 ? kv_dequantize_kernel<VPL, 6> : kv_dequantize_kernel<VPL, 8>;
+  return b == 4 ? kv_dequantize_kernel<VPL, 4, kGpw>
+                : b == 6 ? kv_dequantize_kernel<VPL, 6, kGpw> : kv_dequantize_kernel<VPL, 8, kGpw>;
 }
 
-dim3 grid_for(long long n_groups) { return dim3(static_cast<unsigned>((n_groups + kWarps - 1) / kWarps)); }
+dim3 grid_for(long long n_groups) {
+  return dim3(static_cast<unsigned>((n_groups + kWarps * kGpw - 1) / (kWarps * kGpw)));
+}
 
 }  // namespace
 

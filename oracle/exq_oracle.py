@@ -66,6 +66,16 @@ Readings where the pages are silent (each one is listed in the design doc):
   code, code i at bits [i*b, i*b+b) of the group's little-endian word
   stream, read back as fp16_RNE((u - 2^(b-1)) * s). The integer decisions are
   taken in IEEE fp32 (numpy float32 division and rint), as on the device.
+* EXL2 conversion without calibration data (blog post, "How the EXL2
+  Quantization Pipeline Works Under the Hood", Steps 1-3): the measurement
+  pass runs the model on calibration text, which is out of reach here; it is
+  stood in for by the weight-space squared error of a round-to-nearest
+  quantisation of each 32-row segment at each width (same symmetric RTN
+  arithmetic as the KV codec, one group = one segment of one column). The
+  solve pass follows the printed greedy's increase loop (take the step with
+  the largest error decrease per added bit while the budget allows), started
+  from every segment at the smallest width: started at 4 bits, as printed,
+  it would leave a 4.0 bpw target unmixed. Ties go to the lowest segment.
 """
 from __future__ import annotations
 
@@ -79,6 +89,7 @@ __all__ = [
     "dequant_exl2_definitional", "pack_exl2_qscale", "unpack_exl2_qscale", "exl2_two_level_scales",
     "dequant_exl2_qscale", "matmul", "quantize_rtn", "EXL2_BITS", "SEGMENT_ROWS",
     "KV_BITS", "kv_quantize", "kv_pack", "kv_unpack", "kv_dequantize",
+    "rtn_quantize_exl2", "rtn_errors_exl2", "solve_exl2_bits",
 ]
 
 # ----------------------------------------------------------------------------
@@ -475,6 +486,90 @@ def kv_dequantize(words, scales, b: int, D: int) -> np.ndarray:
     in float64."""
     u = kv_unpack(words, b, D).astype(np.int64) - (1 << (b - 1))
     return fp16_bits_from_float64(u.astype(np.float64) * _as_f64(scales)[:, None])
+
+
+# ----------------------------------------------------------------------------
+# EXL2 conversion: RTN quantizer, weight-space error table, bits solve
+# ----------------------------------------------------------------------------
+
+def _rtn_columns(v32, b: int):
+    """Symmetric RTN of groups along axis 0 (fp32 values): the KV codec's
+    arithmetic. Returns (codes uint8, scale fp16 bits per column)."""
+    qmax = (1 << (b - 1)) - 1
+    amax = np.abs(v32).max(axis=0)
+    s_bits = fp16_bits_from_float64((amax / np.float32(qmax)).astype(np.float64))
+    s = float64_from_fp16_bits(s_bits).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = v32 / s[None, :]
+    q = np.where(s[None, :] == 0, np.float32(0), np.rint(r))
+    q = np.clip(q, -qmax - 1, qmax).astype(np.int64)
+    return (q + (1 << (b - 1))).astype(np.uint8), s_bits
+
+
+def rtn_quantize_exl2(W, perm, bits):
+    """fp16 W [K, N] in input-feature order, perm [K] (stored row j = input
+    row perm[j]) or None, widths [S] -> (codes uint8 [K, N] in stored order,
+    scales uint16 fp16 bits [S, N]) ready for pack_exl2."""
+    Wv = _as_f64(W)
+    if perm is not None:
+        Wv = Wv[np.asarray(perm, dtype=np.int64)]
+    bits = np.asarray(bits, dtype=np.int64)
+    K, N = Wv.shape
+    q = np.zeros((K, N), dtype=np.uint8)
+    s = np.zeros((bits.size, N), dtype=np.uint16)
+    for seg, b in enumerate(bits):
+        rows = slice(seg * SEGMENT_ROWS, (seg + 1) * SEGMENT_ROWS)
+        q[rows], s[seg] = _rtn_columns(Wv[rows].astype(np.float32), int(b))
+    return q, s
+
+
+def rtn_errors_exl2(W, perm) -> np.ndarray:
+    """float64 [S, 6]: sum over the segment's 32 x N weights of (w - w_hat)^2
+    at each width of EXL2_BITS, w_hat the fp16 dequantisation of the RTN codes."""
+    Wv = _as_f64(W)
+    if perm is not None:
+        Wv = Wv[np.asarray(perm, dtype=np.int64)]
+    S = Wv.shape[0] // SEGMENT_ROWS
+    err = np.zeros((S, len(EXL2_BITS)), dtype=np.float64)
+    for seg in range(S):
+        v = Wv[seg * SEGMENT_ROWS:(seg + 1) * SEGMENT_ROWS]
+        for i, b in enumerate(EXL2_BITS):
+            u, s_bits = _rtn_columns(v.astype(np.float32), b)
+            w_hat = float64_from_fp16_bits(fp16_bits_from_float64(
+                (u.astype(np.int64) - (1 << (b - 1))).astype(np.float64) * float64_from_fp16_bits(s_bits)[None, :]))
+            err[seg, i] = np.sum((v - w_hat) ** 2)
+    return err
+
+
+def solve_exl2_bits(err, budget: int) -> np.ndarray:
+    """Widths [S] from the error table [S, 6] and a budget of total code bits
+    per column (sum of widths): every segment starts at 2 bits; while some
+    step to the next width fits the budget, take the one with the largest
+    (err[b] - err[b_next]) / (b_next - b), the lowest segment on ties."""
+    err = np.asarray(err, dtype=np.float64)
+    S = err.shape[0]
+    level = np.zeros(S, dtype=np.int64)          # index into EXL2_BITS
+    widths = np.array(EXL2_BITS, dtype=np.int64)
+    total = 2 * S
+    if budget < total:
+        raise ValueError("budget below two bits per segment")
+    while True:
+        best, best_gain = -1, None
+        for seg in range(S):
+            lv = level[seg]
+            if lv + 1 >= len(widths):
+                continue
+            step = int(widths[lv + 1] - widths[lv])
+            if total + step > budget:
+                continue
+            gain = (err[seg, lv] - err[seg, lv + 1]) / step
+            if best_gain is None or gain > best_gain:
+                best, best_gain = seg, gain
+        if best < 0:
+            break
+        total += int(widths[level[best] + 1] - widths[level[best]])
+        level[best] += 1
+    return widths[level].astype(np.uint8)
 
 
 # ----------------------------------------------------------------------------

@@ -574,3 +574,68 @@ def test_kv_codec_ties_round_to_even():
     u, s = O.kv_quantize(x.astype(np.float16), 4)
     assert int(s[0]) == 0x3092
     assert (u[0, :4].astype(int) - 8).tolist() == [7, 0, 0, 2]
+
+
+# ---------------------------------------------------------------- EXL2 conversion: RTN, errors, solve
+
+def test_rtn_quantize_matches_the_kv_golden_group():
+    # one segment column holding the KV codec's worked group: same scale and codes
+    # (two separately written quantizers against the hand-derived fixture)
+    x, cases = _kv_golden()
+    W = np.zeros((32, 8), dtype=np.uint16)
+    W[:, 3] = x
+    for b, s_want, u_want, _, _ in cases:
+        q, s = O.rtn_quantize_exl2(W, None, [b])
+        assert int(s[0, 3]) == s_want, b
+        assert q[:8, 3].tolist() == u_want, b
+
+
+def test_rtn_quantize_roundtrip_and_errors():
+    rng = np.random.default_rng(21)
+    K, N = 32 * 6, 40
+    W = (rng.standard_normal((K, N)) * 0.02).astype(np.float16)
+    W[:32] *= 8                                   # one loud segment
+    perm = rng.permutation(K).astype(np.int32)
+    err = O.rtn_errors_exl2(W, perm)
+    Wv = O.float64_from_fp16_bits(W.view(np.uint16))
+    for i, b in enumerate(O.EXL2_BITS):
+        bits = np.full(K // 32, b)
+        q, s = O.rtn_quantize_exl2(W, perm, bits)
+        qw, off, sc, pm = O.pack_exl2(q, bits, s.view(np.float16), perm)
+        W_hat = O.float64_from_fp16_bits(O.dequant_exl2(qw, off, bits, sc, pm))
+        # the error table is the squared error of the whole pipeline, per stored segment
+        d2 = ((Wv - W_hat) ** 2)[perm].reshape(K // 32, 32, N).sum(axis=(1, 2))
+        assert np.allclose(err[:, i], d2, rtol=1e-12, atol=0), b
+        # within half a scale step plus half an fp16 ulp of the result
+        sv = O.float64_from_fp16_bits(s)[np.arange(K) // 32][np.argsort(perm)]
+        bound = 0.5 * sv + 0.5 * np.exp2(np.floor(np.log2(np.maximum(np.abs(W_hat), 2.0 ** -14))) - 10)
+        assert (np.abs(Wv - W_hat) <= bound * (1 + 2.0 ** -20)).all(), b
+    assert (np.diff(err, axis=1) <= 0).all()        # more bits, less error (on these weights)
+
+
+def test_solve_exl2_bits_hand_worked():
+    # start 2/2/2 (6 bits); gains per added bit:
+    #   seg2 300 -> 3 bits; seg2 70 -> 4; seg0 50 -> 3; seg0 30 -> 4; seg2 20 -> 5;
+    #   seg0 10 and seg1 10 tie -> seg0 -> 5 (12 bits); then seg1 10 -> 3 (13 bits)
+    err = [[100, 50, 20, 10, 5, 1], [80, 70, 60, 50, 40, 30], [400, 100, 30, 10, 5, 2]]
+    assert O.solve_exl2_bits(err, 6).tolist() == [2, 2, 2]
+    assert O.solve_exl2_bits(err, 8).tolist() == [2, 2, 4]
+    assert O.solve_exl2_bits(err, 12).tolist() == [5, 2, 5]
+    assert O.solve_exl2_bits(err, 13).tolist() == [5, 3, 5]
+    # the 6 -> 8 step costs two bits: taken when they fit, not when one is left
+    one = [[10, 9, 8, 7, 6, 0]]
+    assert O.solve_exl2_bits(one, 8).tolist() == [8]
+    assert O.solve_exl2_bits(one, 7).tolist() == [6]
+    with pytest.raises(ValueError):
+        O.solve_exl2_bits(err, 5)
+
+
+def test_solve_exl2_bits_on_measured_errors():
+    rng = np.random.default_rng(5)
+    K, N = 32 * 16, 64
+    W = (rng.standard_normal((K, N)) * 0.02).astype(np.float16)
+    W[64:96] *= 16                                 # segment 2 is far louder
+    err = O.rtn_errors_exl2(W, None)
+    bits = O.solve_exl2_bits(err, 4 * 16)
+    assert int(bits.astype(int).sum()) == 64 and set(bits.tolist()) <= set(O.EXL2_BITS)
+    assert bits[2] == bits.max() and bits[2] > 4

@@ -71,6 +71,9 @@ def parse_args():
     ap.add_argument("--kv", action="store_true",
                     help="time the quantized KV cache codec (Q4/Q6/Q8 write and read) over a Llama-2-70B cache "
                          "at 32K context instead (one JSON line, GB/s per width and direction)")
+    ap.add_argument("--convert", action="store_true",
+                    help="time the EXL2 conversion (error table, host solve at 4.0 bpw, RTN quantisation) of the "
+                         "Llama-2-70B gate weight instead (one JSON line)")
     ap.add_argument("--kv-groups", type=int, default=80 * 2 * 32768 * 8,
                     help="groups of 128 values for --kv (default: the whole 70B cache at 32K context)")
     ap.add_argument("--decode-sweep", action="store_true",
@@ -494,6 +497,76 @@ def run_kv(args, device):
     }
 
 
+def run_convert(args, device):
+    """EXL2 conversion of one Llama-2-70B gate weight (8192 x 28672 fp16,
+    N(0, 0.02) times a per-row power of two in 2^-2 .. 2^2 and a per-segment
+    one in 2^-3 .. 2^3, a random input permutation): the RTN error table on the GPU, the bits solve on the host
+    for 4.0 bpw, the RTN quantisation on the GPU. CUDA events around `--steps`
+    launches after `--warmup` for the two kernels; wall time for the solve."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    peak, peak_kind = measured_peaks()
+    K, N = synth.LLAMA2_70B_SHAPES["gate"]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(5)
+    W = (torch.randn(K, N, device=device, generator=gen) * 0.02 *
+         torch.exp2(torch.randint(-2, 3, (K, 1), device=device, generator=gen).float())).half()
+    perm = torch.randperm(K, device=device, generator=gen).to(torch.int32)
+    # loudness per stored segment (its 32 input rows), so that the solve has something to allocate
+    loud = torch.exp2(torch.randint(-3, 4, (K // 32,), device=device, generator=gen).float())
+    rows = perm.long()
+    W[rows] = (W[rows].float() * loud.repeat_interleave(32)[:, None]).half()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000 / args.steps
+
+    err = exq.exq_measure_exl2(W, perm)
+    m_us = timed(lambda: exq.exq_measure_exl2(W, perm))
+    t0 = time.perf_counter()
+    bits = exq.exq_solve_exl2_bits(err.cpu().numpy().astype(np.float64), 4 * (K // 32))
+    solve_ms = (time.perf_counter() - t0) * 1000
+    w = exq.exq_quantize_exl2(W, bits, perm)
+    q_us = timed(lambda: exq.exq_quantize_exl2(W, bits, perm))
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the conversion")
+    w_bytes = 2 * K * N
+    packed = w.qweight.numel() * 4 + w.scales.numel() * 2
+    hist = {int(b): int((bits == b).sum()) for b in synth.EXL2_BITS}
+    return {
+        "metric": "EXL2 conversion GB/s (fp16 weight bytes read; quantise: + packed bytes written)",
+        "value": round((w_bytes + packed) / q_us / 1e3, 1),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "dtype": "f16 in, fp32 decisions",
+        "data": "synthetic",
+        "config": {"workload": "convert_70b_gate_4p0bpw", "K": K, "N": N, "value_is": "quantise",
+                   "l2": "inputs larger than L2 (470 MB of fp16)"},
+        "roofline": {"bound": "hbm", "peak": peak, "unit": UNIT, "peak_kind": peak_kind},
+        "measure": {"us": round(m_us, 1), "GB/s": round(w_bytes / m_us / 1e3, 1),
+                    "frac": round(w_bytes / m_us / 1e3 / peak, 4), "widths_tried": 6},
+        "solve": {"ms": round(solve_ms, 2), "segments": K // 32, "budget_bits": 4 * (K // 32), "widths": hist},
+        "quantize": {"us": round(q_us, 1), "GB/s": round((w_bytes + packed) / q_us / 1e3, 1),
+                     "frac": round((w_bytes + packed) / q_us / 1e3 / peak, 4)},
+    }
+
+
 def max_over_ranks(times, world, device=None):
     """The slowest rank's times: every rank waits for all of them (all-reduce
     MAX over the process group; a CPU tensor under gloo)."""
@@ -748,6 +821,10 @@ def main():
     if args.prefill:
         if rank == 0:
             print(json.dumps(run_prefill(args, torch.device("cuda", local))), flush=True)
+        return
+    if args.convert:
+        if rank == 0:
+            print(json.dumps(run_convert(args, torch.device("cuda", local))), flush=True)
         return
     if args.kv:
         if rank == 0:

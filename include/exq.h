@@ -297,6 +297,58 @@ exq_status exq_kv_quantize(const uint16_t* x, int64_t n_groups, int32_t D, int32
 exq_status exq_kv_dequantize(const uint32_t* codes, const uint16_t* scales, int64_t n_groups, int32_t D,
                              int32_t bits, uint16_t* x_out, void* stream);
 
+/* ---------------------------------------------------------------- EXL2 conversion */
+
+/* Converting an fp16 weight to EXL2 without calibration data (ExLlamaV2 blog
+ * post, "How the EXL2 Quantization Pipeline Works Under the Hood": Step 1
+ * measures each layer at every width, Step 2 solves for a width per group at a
+ * target bpw, Step 3 quantises). The measurement on calibration text is out of
+ * reach here; it is stood in for by the weight-space squared error of a
+ * round-to-nearest quantisation. The quantiser is symmetric per (32-row
+ * segment, column), qmax = 2^(b-1) - 1:
+ *   s = fp16_RNE(fp32_RNE(amax / qmax)),
+ *   q = clamp(rint(fp32_RNE(w / s)), -qmax - 1, qmax)   (q = 0 where s = 0),
+ *   stored code u = q + 2^(b-1), i.e. the EXL2 dequantisation gives back
+ *   fp16_RNE(q * s). */
+
+/* exq_quantize_exl2 -- device, asynchronous.
+ *   W            device fp16 [K, N], input-feature order
+ *   perm         device int32 [K] (stored row j holds input row perm[j]) or NULL
+ *   seg_word_off device uint32 [K/32 + 1]: the widths as prefix sums (see the
+ *                EXL2 layout; exq_pack_exl2 returns them, or build them from
+ *                the solve's widths)
+ *   n_word_rows  seg_word_off[K/32] (rows of qweight_out)
+ *   qweight_out  device uint32 [n_word_rows, N], scales_out device fp16 [K/32, N]
+ * The result is an EXL2 layer (with perm) for exq_gemv / exq_gemm / exq_dequant.
+ * A width outside the set, or offsets past n_word_rows, leave that segment
+ * unwritten and set EXQ_ERR_INVALID_ARG in the device error word; so do
+ * permutation entries outside [0, K) (read as 0). */
+exq_status exq_quantize_exl2(const uint16_t* W, const int32_t* perm, int32_t K, int32_t N,
+                             const uint32_t* seg_word_off, int32_t n_word_rows, uint32_t* qweight_out,
+                             uint16_t* scales_out, void* stream);
+
+/* Bytes of device workspace exq_measure_exl2 needs (0 for bad K, N). */
+size_t exq_measure_exl2_workspace_size(int32_t K, int32_t N);
+
+/* exq_measure_exl2 -- device, asynchronous: err_out fp32 [K/32, 6], the sum
+ * over a segment's 32 x N weights of (w - w_hat)^2 at widths 2, 3, 4, 5, 6, 8
+ * (w_hat the fp16 dequantisation of the RTN codes above). fp32 sums in a
+ * fixed order: deterministic. Same W / perm rules as exq_quantize_exl2. */
+exq_status exq_measure_exl2(const uint16_t* W, const int32_t* perm, int32_t K, int32_t N, float* err_out,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* exq_solve_exl2_bits -- host, synchronous: widths for a budget of code bits.
+ *   err     host double [S, 6], the error table (exq_measure_exl2's, or any)
+ *   budget  total code bits per column, sum of the widths (e.g. bpw * S)
+ *   bits_out host uint8 [S]
+ * Every segment starts at 2 bits; while some step to the next width (2, 3,
+ * 4, 5, 6, 8) fits the budget, the step with the largest
+ * (err[b] - err[b_next]) / (b_next - b) is taken, the lowest segment on
+ * ties (the increase loop of the blog post's Step 2 greedy, started from the
+ * smallest width). Returns EXQ_ERR_INVALID_ARG for NULL buffers, S <= 0 or a
+ * budget below 2 * S. */
+exq_status exq_solve_exl2_bits(const double* err, int32_t S, int64_t budget, uint8_t* bits_out);
+
 /* ---------------------------------------------------------------- status */
 
 /* Static, NUL-terminated description of a status code. */

@@ -16,7 +16,7 @@ CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libexq.so"
 
-SOURCES = ["exq_api.cu", "exq_gemv.cu", "exq_dequant.cu", "exq_gemm.cu", "exq_kv.cu", "exq_pack.cpp"]
+SOURCES = ["exq_api.cu", "exq_gemv.cu", "exq_dequant.cu", "exq_gemm.cu", "exq_kv.cu", "exq_convert.cu", "exq_pack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -203,6 +203,44 @@ extern "C" exq_status exq_kv_dequantize(const uint32_t* codes, const uint16_t* s
   return launch_kv_dequantize(codes, scales, n_groups, D, bits, x_out, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+exq_status check_convert(const uint16_t* W, const int32_t* perm, int K, int N) {
+  if (!W || !aligned16(W) || (perm && !aligned16(perm))) return EXQ_ERR_INVALID_ARG;
+  if (K <= 0 || N <= 0 || K % 32 || N % 8) return EXQ_ERR_INVALID_ARG;
+  return EXQ_OK;
+}
+}  // namespace
+
+extern "C" exq_status exq_quantize_exl2(const uint16_t* W, const int32_t* perm, int32_t K, int32_t N,
+                                        const uint32_t* seg_word_off, int32_t n_word_rows, uint32_t* qweight_out,
+                                        uint16_t* scales_out, void* stream) {
+  const exq_status st = check_convert(W, perm, K, N);
+  if (st != EXQ_OK) return st;
+  if (!seg_word_off || !qweight_out || !scales_out || !aligned16(seg_word_off) || !aligned16(qweight_out) ||
+      !aligned16(scales_out))
+    return EXQ_ERR_INVALID_ARG;
+  if (n_word_rows < 2 * (K / 32) || n_word_rows > 8 * (K / 32)) return EXQ_ERR_INVALID_ARG;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_rtn_quantize(W, perm, K, N, seg_word_off, n_word_rows, qweight_out, scales_out,
+                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t exq_measure_exl2_workspace_size(int32_t K, int32_t N) {
+  if (K <= 0 || N <= 0 || K % 32 || N % 8) return 0;
+  return measure_workspace_bytes(K, N);
+}
+
+extern "C" exq_status exq_measure_exl2(const uint16_t* W, const int32_t* perm, int32_t K, int32_t N, float* err_out,
+                                       void* workspace, size_t ws_bytes, void* stream) {
+  const exq_status st = check_convert(W, perm, K, N);
+  if (st != EXQ_OK) return st;
+  if (!err_out || !aligned16(err_out) || !workspace || !aligned16(workspace) ||
+      ws_bytes < measure_workspace_bytes(K, N))
+    return EXQ_ERR_INVALID_ARG;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_rtn_measure(W, perm, K, N, err_out, workspace, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" const char* exq_status_string(exq_status s) {
   switch (s) {
     case EXQ_OK: return "ok";
@@ -216,9 +254,10 @@ extern "C" const char* exq_status_string(exq_status s) {
 
 extern "C" exq_status exq_get_last_device_error(void* stream) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const unsigned a = take_gemv_errors(s), b = take_dequant_errors(s), c = take_gemm_errors(s);
-  if (a == ~0u || b == ~0u || c == ~0u) return EXQ_ERR_CUDA;
-  const unsigned v = a | b | c;
+  const unsigned a = take_gemv_errors(s), b = take_dequant_errors(s), c = take_gemm_errors(s),
+                 d = take_convert_errors(s);
+  if (a == ~0u || b == ~0u || c == ~0u || d == ~0u) return EXQ_ERR_CUDA;
+  const unsigned v = a | b | c | d;
   if (v & kDevErrTimeout) return EXQ_ERR_TIMEOUT;
   if (v & (kDevErrBadSegment | kDevErrBadPerm)) return EXQ_ERR_INVALID_ARG;
   return EXQ_OK;

@@ -185,6 +185,17 @@ __device__ __forceinline__ uint32_t two_level_scale2(uint32_t cc, uint32_t m2) {
   return hmul2(f, m2);
 }
 
+// x / s rounded to an integer as rint(fp32_RN(x / s)): the quotient comes
+// from a multiply by fp32_RN(1 / s), which is within 3 * 2^-24 |x / s| of the
+// correctly rounded one; only where that leaves the quotient within 2^-14 of
+// a half-integer (|x / s| <= 256: 4.6e-5 < 2^-14) does the exact division
+// decide. Beyond 256 the code is clamped whichever quotient is used.
+__device__ __forceinline__ int round_quotient(float x, float s, float inv) {
+  float r = x * inv;
+  if (fabsf(fabsf(r - rintf(r)) - 0.5f) < 0x1p-14f) r = __fdiv_rn(x, s);
+  return __float2int_rn(r);
+}
+
 // Bit-window of one 8-code block: block t (0..3) of a segment of width b
 // starts at stream bit 8 t b. Returns the first word row (relative to the
 // segment) and the bit offset inside it.

@@ -56,10 +56,18 @@ exq_status launch_kv_quantize(const uint16_t* x, long long n_groups, int D, int 
 exq_status launch_kv_dequantize(const uint32_t* codes, const uint16_t* scales, long long n_groups, int D, int b,
                                 uint16_t* x_out, cudaStream_t stream);
 
+// EXL2 conversion: RTN quantiser into the EXL2 layout, and the error table
+exq_status launch_rtn_quantize(const uint16_t* W, const int32_t* perm, int K, int N, const uint32_t* seg_off,
+                               int n_word_rows, uint32_t* qweight, uint16_t* scales, cudaStream_t stream);
+exq_status launch_rtn_measure(const uint16_t* W, const int32_t* perm, int K, int N, float* err, void* workspace,
+                              cudaStream_t stream);
+size_t measure_workspace_bytes(int K, int N);
+
 // read-and-clear of each module's device error word (stream-ordered copy +
 // synchronise); returns the OR of the codes or ~0u on a CUDA failure
 unsigned take_gemv_errors(cudaStream_t stream);
 unsigned take_dequant_errors(cudaStream_t stream);
 unsigned take_gemm_errors(cudaStream_t stream);
+unsigned take_convert_errors(cudaStream_t stream);
 
 }  // namespace exq

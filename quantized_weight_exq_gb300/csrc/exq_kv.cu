@@ -52,17 +52,6 @@ __device__ __forceinline__ void unpack_halves(const typename Vec<VPL>::T& v, uin
   }
 }
 
-// x / s rounded to an integer as rint(fp32_RN(x / s)): the quotient comes
-// from a multiply by fp32_RN(1 / s), which is within 3 * 2^-24 |x / s| of the
-// correctly rounded one; only where that leaves the quotient within 2^-14 of
-// a half-integer (|x / s| <= 256: 4.6e-5 < 2^-14) does the exact division
-// decide. Beyond 256 the code is clamped whichever quotient is used.
-__device__ __forceinline__ int round_quotient(float x, float s, float inv) {
-  float r = x * inv;
-  if (fabsf(fabsf(r - rintf(r)) - 0.5f) < 0x1p-14f) r = __fdiv_rn(x, s);
-  return __float2int_rn(r);
-}
-
 template <int VPL, int B, int GPW>
 __global__ void __launch_bounds__(kWarps * 32)
     kv_quantize_kernel(const uint16_t* __restrict__ x, long long n_groups, uint32_t* __restrict__ codes,

@@ -10,6 +10,9 @@
 //
 // EXL2: 32-row segments at widths {2,3,4,5,6,8} (README, "EXL2
 // quantization"); each segment-column is a 32*b-bit little-endian stream.
+#include <queue>
+#include <utility>
+#include <vector>
 #include <cstdint>
 #include <cstring>
 #include <vector>
@@ -126,5 +129,38 @@ extern "C" exq_status exq_pack_exl2_qscale(const uint8_t* codes, int32_t S, int3
       }
       q_scale_out[s * (N / 8) + k] = word;
     }
+  return EXQ_OK;
+}
+
+// Widths for a budget of code bits: from 2 bits everywhere, repeatedly the
+// step with the largest error decrease per added bit that still fits, the
+// lowest segment on ties. A step that does not fit never will (the room only
+// shrinks), so it leaves the queue for good.
+extern "C" exq_status exq_solve_exl2_bits(const double* err, int32_t S, int64_t budget, uint8_t* bits_out) {
+  static const int kW[6] = {2, 3, 4, 5, 6, 8};
+  if (!err || !bits_out || S <= 0 || budget < 2 * static_cast<int64_t>(S)) return EXQ_ERR_INVALID_ARG;
+  std::vector<int> level(S, 0);
+  // (gain, -segment): the largest gain first, then the lowest segment
+  using Item = std::pair<double, int32_t>;
+  std::priority_queue<Item> heap;
+  auto push = [&](int32_t s) {
+    const int lv = level[s];
+    if (lv + 1 < 6) heap.push({(err[6 * static_cast<int64_t>(s) + lv] - err[6 * static_cast<int64_t>(s) + lv + 1]) /
+                                   (kW[lv + 1] - kW[lv]),
+                               -s});
+  };
+  for (int32_t s = 0; s < S; ++s) push(s);
+  int64_t total = 2 * static_cast<int64_t>(S);
+  while (!heap.empty()) {
+    const Item top = heap.top();
+    heap.pop();
+    const int32_t s = -top.second;
+    const int step = kW[level[s] + 1] - kW[level[s]];
+    if (total + step > budget) continue;
+    total += step;
+    ++level[s];
+    push(s);
+  }
+  for (int32_t s = 0; s < S; ++s) bits_out[s] = static_cast<uint8_t>(kW[level[s]]);
   return EXQ_OK;
 }

@@ -32,6 +32,7 @@ EXPORTED = (
     "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
     "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error", "exq_kv_quantize", "exq_kv_dequantize",
+    "exq_quantize_exl2", "exq_measure_exl2_workspace_size", "exq_measure_exl2", "exq_solve_exl2_bits",
 )
 
 # most layers one exq_gemv_multi call takes (EXQ_GEMV_MAX_LAYERS)
@@ -79,6 +80,10 @@ def _load():
         "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
         "exq_kv_quantize": (st, [P, i64, i32, i32, P, P, P]),
         "exq_kv_dequantize": (st, [P, P, i64, i32, i32, P, P]),
+        "exq_quantize_exl2": (st, [P, P, i32, i32, P, i32, P, P, P]),
+        "exq_measure_exl2_workspace_size": (sz, [i32, i32]),
+        "exq_measure_exl2": (st, [P, P, i32, i32, P, P, sz, P]),
+        "exq_solve_exl2_bits": (st, [P, i32, i64, P]),
         "exq_status_string": (ctypes.c_char_p, [st]),
         "exq_get_last_device_error": (st, [P]),
     }
@@ -349,6 +354,45 @@ def exq_kv_dequantize(codes, scales, D: int, bits: int, out=None, stream=None):
     _check(_lib.exq_kv_dequantize(codes.data_ptr(), scales.data_ptr(), G, D, bits, out.data_ptr(),
                                   _stream_ptr(stream)), "exq_kv_dequantize")
     return out
+
+
+def exq_solve_exl2_bits(err: np.ndarray, budget: int) -> np.ndarray:
+    """Host: widths uint8 [S] for an error table float64 [S, 6] and a budget of
+    code bits per column."""
+    err = np.ascontiguousarray(err, dtype=np.float64)
+    S = err.shape[0]
+    out = np.empty(S, dtype=np.uint8)
+    _check(_lib.exq_solve_exl2_bits(_np_ptr(err), S, int(budget), _np_ptr(out)), "exq_solve_exl2_bits")
+    return out
+
+
+def exq_measure_exl2(W, perm=None, stream=None):
+    """RTN error table fp32 [K/32, 6] of an fp16 weight [K, N] (device)."""
+    import torch
+    K, N = W.shape
+    err = torch.empty(K // 32, 6, dtype=torch.float32, device=W.device)
+    nws = int(_lib.exq_measure_exl2_workspace_size(K, N))
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=W.device)
+    _check(_lib.exq_measure_exl2(W.data_ptr(), None if perm is None else perm.data_ptr(), K, N, err.data_ptr(),
+                                 ws.data_ptr(), nws, _stream_ptr(stream)), "exq_measure_exl2")
+    return err
+
+
+def exq_quantize_exl2(W, bits, perm=None, stream=None) -> Weight:
+    """RTN conversion of an fp16 weight [K, N] (device) at the given widths
+    [K/32] into an EXL2 layer."""
+    import torch
+    K, N = W.shape
+    bits = np.asarray(bits, dtype=np.int64)
+    off = np.zeros(bits.size + 1, dtype=np.int64)
+    off[1:] = np.cumsum(bits)
+    rows = int(off[-1])
+    off_d = torch.from_numpy(off.astype(np.int32)).to(W.device)
+    qw = torch.empty(rows, N, dtype=torch.int32, device=W.device)
+    sc = torch.empty(K // 32, N, dtype=torch.float16, device=W.device)
+    _check(_lib.exq_quantize_exl2(W.data_ptr(), None if perm is None else perm.data_ptr(), K, N, off_d.data_ptr(),
+                                  rows, qw.data_ptr(), sc.data_ptr(), _stream_ptr(stream)), "exq_quantize_exl2")
+    return Weight(EXQ_FMT_EXL2, K, N, 32, qw, sc, None, perm, off_d)
 
 
 def exq_get_last_device_error(stream=None) -> int:

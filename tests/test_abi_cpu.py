@@ -215,3 +215,34 @@ def test_kv_codec_validates_on_host(exq):
         assert f(b=0x60008) == exq.EXQ_ERR_INVALID_ARG
         assert f(c=None) == exq.EXQ_ERR_INVALID_ARG
         assert f(G=0, a=None, b=None, c=None) == exq.EXQ_OK   # nothing to do, no launch
+
+
+def test_solve_exl2_bits_matches_oracle(exq):
+    err = np.array([[100, 50, 20, 10, 5, 1], [80, 70, 60, 50, 40, 30], [400, 100, 30, 10, 5, 2]], np.float64)
+    for budget in (6, 8, 12, 13, 24):
+        assert np.array_equal(exq.exq_solve_exl2_bits(err, budget), O.solve_exl2_bits(err, budget)), budget
+    rng = np.random.default_rng(9)
+    for S in (1, 7, 64, 300):
+        # decreasing error curves with ties sprinkled in
+        e = np.sort(rng.random((S, 6)) * rng.integers(1, 4, (S, 1)), axis=1)[:, ::-1].copy()
+        e[::5] = e[0]
+        for bpw in (2.0, 2.5, 3.3, 4.0, 5.1, 8.0):
+            budget = int(round(bpw * S))
+            assert np.array_equal(exq.exq_solve_exl2_bits(e, budget), O.solve_exl2_bits(e, budget)), (S, bpw)
+    with pytest.raises(exq.ExqError):
+        exq.exq_solve_exl2_bits(err, 5)
+
+
+def test_convert_validates_on_host(exq):
+    from quantized_weight_exq_gb300 import exq as mod
+    lib = mod._lib
+    assert lib.exq_measure_exl2_workspace_size(100, 64) == 0
+    assert lib.exq_measure_exl2_workspace_size(64, 60) == 0
+    ws = lib.exq_measure_exl2_workspace_size(64, 512)
+    assert ws == 2 * 2 * 6 * 4                        # 2 segments x 2 column blocks x 6 widths, fp32
+    assert lib.exq_measure_exl2(0x10000, None, 64, 512, 0x20000, 0x30000, ws - 4, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_measure_exl2(0x10002, None, 64, 512, 0x20000, 0x30000, ws, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_measure_exl2(0x10000, None, 60, 512, 0x20000, 0x30000, ws, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_quantize_exl2(0x10000, None, 64, 512, None, 8, 0x20000, 0x30000, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_quantize_exl2(0x10000, None, 64, 512, 0x40000, 3, 0x20000, 0x30000, None) == exq.EXQ_ERR_INVALID_ARG
+    assert lib.exq_quantize_exl2(0x10000, 0x50004, 64, 512, 0x40000, 8, 0x20000, 0x30000, None) == exq.EXQ_ERR_INVALID_ARG

@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--format", default="exl2", choices=["exl2", "exl2_qscale"],
                     help="decode stream format: EXL2 4.0 bpw with fp16 scales (default) or with two-level "
                          "scales (4-bit group-scale codes x per-column fp16 maxima)")
+    ap.add_argument("--segment-order", default="random", choices=["random", "sorted"],
+                    help="stored order of a layer's EXL2 segments: as drawn, or grouped by width (the row "
+                         "remapping lays out equal widths contiguously)")
     ap.add_argument("--ungrouped", action="store_true",
                     help="decode stream as one exq_gemv per linear (each with its own x) instead of grouping "
                          "the linears that share x (q/k/v, gate/up) into exq_gemv_multi calls")
@@ -165,7 +168,8 @@ def bit_mix(layer: int, lin: int, K: int):
     return synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, synth.rng_for(0, wid, 7 * layer + lin, 4))
 
 
-def build_stream(exq, torch, layers: int, device, grouped: bool = True, two_level: bool = False):
+def build_stream(exq, torch, layers: int, device, grouped: bool = True, two_level: bool = False,
+                 sorted_widths: bool = False):
     """Device-resident packed weights for the whole stream, as a list of
     calls (weights, x, outputs). Packed codes are uniform random words (a
     segment column's b words are a bijection of its 32 uniform b-bit codes);
@@ -189,7 +193,10 @@ def build_stream(exq, torch, layers: int, device, grouped: bool = True, two_leve
                 K, N = synth.LLAMA2_70B_SHAPES[name]
                 gen = torch.Generator(device=device)
                 gen.manual_seed(int(synth.rng_for(0, wid, 7 * layer + i, 0).integers(0, 2 ** 62)))
-                ws.append(exl2_device_layer(exq, torch, K, N, bit_mix(layer, i, K), gen, device, two_level))
+                bits = bit_mix(layer, i, K)
+                if sorted_widths:  # equal widths stored contiguously (the permutation absorbs the order)
+                    bits = np.sort(bits)[::-1].copy()
+                ws.append(exl2_device_layer(exq, torch, K, N, bits, gen, device, two_level))
                 if x is None:  # the group's activations: drawn with its first linear's generator
                     x = x_all[xo:xo + K].view(1, K)
                     x.copy_(torch.randn(1, K, device=device, generator=gen).half())
@@ -595,7 +602,8 @@ def run_exq(args, rank, world, device):
     torch.cuda.set_device(device)
     grouped = not args.ungrouped
     two_level = args.format == "exl2_qscale"
-    calls, x_all, y_all = build_stream(exq, torch, args.layers, device, grouped=grouped, two_level=two_level)
+    calls, x_all, y_all = build_stream(exq, torch, args.layers, device, grouped=grouped, two_level=two_level,
+                                       sorted_widths=args.segment_order == "sorted")
     per_layer = len(calls) // args.layers
     bytes_per_step = sum(w.packed_bytes for ws_, _, _ in calls for w in ws_)
     n_linears = sum(len(ws_) for ws_, _, _ in calls)
@@ -692,6 +700,7 @@ def run_exq(args, rank, world, device):
             "workload": "decode_stream_70b_exl2_4p0bpw" + ("_two_level_scales" if two_level else ""),
             "model_shape": "Llama-2-70B (80 layers x q,k,v,o,gate,up,down)",
             "scales": "4-bit group-scale codes x fp16 column maxima" if two_level else "fp16 per (segment, column)",
+            "segment_order": args.segment_order,
             "layers": args.layers,
             "M": 1,
             "bpw": 4.0,

@@ -57,6 +57,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "exq_device.cuh"
 #include "exq_internal.h"
@@ -149,7 +150,7 @@ __device__ __forceinline__ GemvLayer layer_params(const GemvArgs& a, int L) {
 // Stage descriptor, written by the producer before the slot's copies.
 // The consumer K groups take the first h = (count + 1) / 2 segments and the rest.
 //   a: first segment | count << 16 | first-of-piece << 20 | last-of-piece << 21
-//      | end << 22 | H << 24, H = the second half's first word row in the slot
+//      | end << 22 | uniform width << 23 | H << 24, H = the second half's first word row in the slot
 //      (EXL2) or its scale / zero row (GPTQ)
 //   b: EXL2: widths, 4 bits per segment (0 = skip the segment);
 //      GPTQ: position in its group of the first segment | of the second half's << 16
@@ -159,6 +160,7 @@ struct Desc {
   uint32_t a, b, c, d;
 };
 constexpr uint32_t kDescFirst = 1u << 20, kDescLast = 1u << 21, kDescEnd = 1u << 22;
+constexpr uint32_t kDescUniform = 1u << 23;  // EXL2: every segment of the stage has the same width
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -584,7 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           half = static_cast<uint32_t>(__shfl_sync(0xffffffffu, ps_h, h - 1));
           db = widths;
         }
+        bool uniform = false;
+        if constexpr (FMT != EXQ_FMT_GPTQ4) {
+          const uint32_t b0 = widths & 15u;
+          const uint32_t used = n >= 8 ? ~0u : (1u << (4 * n)) - 1u;
+          uniform = !bad && ((widths ^ (b0 * 0x11111111u)) & used) == 0;
+        }
         const uint32_t da = static_cast<uint32_t>(seg) | (static_cast<uint32_t>(n) << 16) | (first ? kDescFirst : 0u) |
+                            (uniform ? kDescUniform : 0u) |
                             (last ? kDescLast : 0u) | (half << 24);
         ok = issue(da, db, tile, lt, row0, srow, bad);
         seg += n;
@@ -638,6 +647,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint2 mv = make_uint2(0u, 0u);
       if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) mv = lds64(sl + kSlotS + col_off);
       int o = kg ? static_cast<int>(d.a >> 24) : 0;  // word row of segment j0 in the slot
+      // a stage of one width: the width is known for the whole run
+      auto run = [&](auto width) {
+        constexpr int B = decltype(width)::value;
+        for (int j = j0; j < j1; ++j, o += B) {
+          uint32_t xb[MT][4];
+          x_pairs(xrow0 + 64 * j, xb[0]);
+          if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+          if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+            qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
+          else
+            scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
+          const int bit = 8 * B * t;
+          exl2_seg<B, MT>(wrow + (o + (bit >> 5)) * kRowBytes, static_cast<uint32_t>(bit & 31), xb, s2, acc);
+        }
+      };
+      if (d.a & kDescUniform) {
+        switch (widths & 15u) {
+          case 2: run(std::integral_constant<int, 2>{}); break;
+          case 3: run(std::integral_constant<int, 3>{}); break;
+          case 4: run(std::integral_constant<int, 4>{}); break;
+          case 5: run(std::integral_constant<int, 5>{}); break;
+          case 6: run(std::integral_constant<int, 6>{}); break;
+          default: run(std::integral_constant<int, 8>{}); break;
+        }
+      } else
       for (int j = j0; j < j1; ++j) {
         const int b = static_cast<int>((widths >> (4 * j)) & 15u);
         if (b != 0) {  // 0: a segment the producer rejected (reported)

@@ -282,3 +282,45 @@ def test_decode_stream_70b_sampled(env, name):
     assert np.array_equal(_dequant(exq, torch, w)[:, cols], W_ref)
     x = synth.activations(1, K, seed=7, workload=wid)
     check_matmul(_gemv(exq, torch, w, x)[:, cols], O.matmul(x, W_ref), f"70b {name}")
+
+
+# ---------------------------------------------------------------- size limits and degenerate shapes
+
+def test_gemv_single_segment(env):
+    # K = 32: one segment, one stage, every CTA but one idle
+    exq, torch = env
+    for bits in (np.array([2]), np.array([3]), np.array([8])):
+        e = exl2_case(32, 200, bits=bits, permute=True, seed=int(bits[0]))
+        for M in (1, 16):
+            x = synth.activations(M, 32, seed=M)
+            check_matmul(_gemv(exq, torch, _exl2_dev(exq, e), x), O.matmul(x, oracle_W_exl2(e)), f"K=32 b={bits}")
+    g = gptq_case(32, 64, 32, act_order=True, seed=2)
+    x = synth.activations(3, 32, seed=3)
+    check_matmul(_gemv(exq, torch, _gptq_dev(exq, g), x), O.matmul(x, oracle_W_gptq(g)), "gptq K=32")
+
+
+def test_gemv_widest_layer(env):
+    # the most columns one call takes: 2048 tiles of 248 (N = 507,904), K = 64;
+    # sampled columns against the oracle, the last tile included
+    exq, torch = env
+    N = 2048 * 248
+    e = exl2_case(64, N, bits=np.array([4, 6]), permute=False, seed=5)
+    w = _exl2_dev(exq, e)
+    x = synth.activations(1, 64, seed=5)
+    cols = np.unique(np.concatenate([np.random.default_rng(5).choice(N, 300, replace=False), np.arange(N - 300, N)]))
+    check_matmul(_gemv(exq, torch, w, x)[:, cols], O.matmul(x, oracle_W_exl2(e, cols=cols)), "N = 507904")
+    # one more tile is past the counter region
+    e2 = exl2_case(64, N + 8, bits=np.array([4, 4]), permute=False, seed=6)
+    assert exq.exq_gemv_workspace_size(_exl2_dev(exq, e2), 1) == 0
+
+
+def test_gemv_deepest_layer(env):
+    # the longest K segment indices allow: 65535 segments (K = 2,097,120), N = 8
+    exq, torch = env
+    K = 65535 * 32
+    g = gptq_case(K, 8, 32, act_order=False, seed=7)
+    w = _gptq_dev(exq, g)
+    x = synth.activations(1, K, seed=7)
+    check_matmul(_gemv(exq, torch, w, x), O.matmul(x, oracle_W_gptq(g)), "K = 2097120")
+    g2 = gptq_case(K + 32, 8, 32, act_order=False, seed=8)
+    assert exq.exq_gemv_workspace_size(_gptq_dev(exq, g2), 1) == 0

@@ -52,6 +52,54 @@ __device__ __forceinline__ void unpack_halves(const typename Vec<VPL>::T& v, uin
   }
 }
 
+constexpr int gcd32(int c) { return c % 32 == 0 ? 32 : c % 16 == 0 ? 16 : c % 8 == 0 ? 8 : 4; }
+
+// The group's code words from the lanes' bit chunks (lane l holds stream bits
+// [l C, l C + C), C = kChunk <= 64): word w gathers, by warp shuffles, the at
+// most NC chunks that overlap bits [32 w, 32 w + 32). Every lane calls it.
+template <int kChunk, int kWords>
+__device__ __forceinline__ void store_words(unsigned long long chunk, uint32_t* __restrict__ dst, int lane) {
+  if constexpr (kChunk == 64) {  // two whole words per lane
+    *reinterpret_cast<uint2*>(dst + 2 * lane) =
+        make_uint2(static_cast<uint32_t>(chunk), static_cast<uint32_t>(chunk >> 32));
+    return;
+  } else if constexpr (kChunk == 32) {  // one whole word per lane
+    dst[lane] = static_cast<uint32_t>(chunk);
+    return;
+  } else if constexpr (kChunk == 16 || kChunk == 8) {  // 32 / kChunk lanes fill a word
+    constexpr int kPer = 32 / kChunk;
+    uint32_t word = static_cast<uint32_t>(chunk);
+#pragma unroll
+    for (int i = 1; i < kPer; ++i)
+      word |= __shfl_down_sync(0xffffffffu, static_cast<uint32_t>(chunk), i) << (i * kChunk);
+    if (lane % kPer == 0) dst[lane / kPer] = word;
+    return;
+  }
+  constexpr int NC = (kChunk - gcd32(kChunk) + 32 + kChunk - 1) / kChunk;
+#pragma unroll
+  for (int r = 0; r < (kWords + 31) / 32; ++r) {
+    const int w = 32 * r + lane;
+    const int l0 = min(32 * w / kChunk, 31);
+    const int sh = 32 * w - l0 * kChunk;  // the word's first bit inside chunk l0
+    uint32_t word = 0;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int src = min(l0 + c, 31);
+      unsigned long long v;
+      if constexpr (kChunk <= 32) {
+        v = __shfl_sync(0xffffffffu, static_cast<uint32_t>(chunk), src);
+      } else {
+        const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(chunk), src);
+        const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(chunk >> 32), src);
+        v = (static_cast<unsigned long long>(hi) << 32) | lo;
+      }
+      const int pos = c * kChunk - sh;  // chunk l0 + c starts this many bits into the word
+      if (l0 + c <= 31 && pos < 32) word |= pos >= 0 ? static_cast<uint32_t>(v << pos) : static_cast<uint32_t>(v >> -pos);
+    }
+    if (w < kWords) dst[w] = word;
+  }
+}
+
 template <int VPL, int B, int GPW>
 __global__ void __launch_bounds__(kWarps * 32)
     kv_quantize_kernel(const uint16_t* __restrict__ x, long long n_groups, uint32_t* __restrict__ codes,
@@ -60,7 +108,6 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int kWords = D * B / 32;   // words of a group
   constexpr int kChunk = VPL * B;      // bits of one lane (8..64)
   constexpr int kQmax = (1 << (B - 1)) - 1;
-  __shared__ uint32_t words[kWarps][GPW][kWords];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the block's groups: k * kWarps + warp, k < GPW (each k a contiguous run of kWarps groups)
   const long long g0 = static_cast<long long>(blockIdx.x) * kWarps * GPW + warp;
@@ -72,10 +119,6 @@ __global__ void __launch_bounds__(kWarps * 32)
     const long long g = g0 + k * kWarps;
     if (g < n_groups) raw[k] = *reinterpret_cast<const V*>(x + g * D + lane * VPL);
   }
-#pragma unroll
-  for (int k = 0; k < GPW; ++k)
-    for (int i = lane; i < kWords; i += 32) words[warp][k][i] = 0u;
-  __syncwarp();
 
 #pragma unroll
   for (int k = 0; k < GPW; ++k) {
@@ -103,19 +146,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (s != 0.f) q = max(-kQmax - 1, min(kQmax, round_quotient(xf[i], s, inv)));
       chunk |= static_cast<unsigned long long>(q + (1 << (B - 1))) << (i * B);
     }
-    // the lane's bits sit at stream offset lane * kChunk and touch at most two words
-    const int off = lane * kChunk;
-    const unsigned long long win = chunk << (off & 31);
-    atomicOr(&words[warp][k][off >> 5], static_cast<uint32_t>(win));
-    if ((off & 31) + kChunk > 32) atomicOr(&words[warp][k][(off >> 5) + 1], static_cast<uint32_t>(win >> 32));
+    store_words<kChunk, kWords>(chunk, codes + g * kWords, lane);
     if (lane == 0) scales[g] = __half_as_ushort(s16);
-  }
-  __syncwarp();
-#pragma unroll
-  for (int k = 0; k < GPW; ++k) {
-    const long long g = g0 + k * kWarps;
-    if (g >= n_groups) break;
-    for (int i = lane; i < kWords; i += 32) codes[g * kWords + i] = words[warp][k][i];
   }
 }
 

@@ -346,7 +346,18 @@ __device__ __forceinline__ void zero4(float (&a)[MT][2][4]) {
 }
 
 // the pairs (x0,x4),(x1,x5),(x2,x6),(x3,x7) of 8 consecutive activations
+// (from natural order; with XP the gather already stored each 8-block as
+// x0 x4 x1 x5 x2 x6 x3 x7, so the words are the pairs)
+template <bool XP>
 __device__ __forceinline__ void x_pairs(const uint8_t* p, uint32_t (&xb)[4]) {
+  if constexpr (XP) {
+    const uint4 v = lds128(p);
+    xb[0] = v.x;
+    xb[1] = v.y;
+    xb[2] = v.z;
+    xb[3] = v.w;
+    return;
+  }
   const uint4 v = lds128(p);
   xb[0] = prmt(v.x, v.z, 0x5410);
   xb[1] = prmt(v.x, v.z, 0x7632);
@@ -397,7 +408,10 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restric
   if (!in) return;
   const bool ok = static_cast<unsigned>(p) < static_cast<unsigned>(K);
   if (!ok) atomicOr(&g_gemv_err, kDevErrBadPerm);
-  xp[static_cast<size_t>(l) * M * K + e] = ok ? __ldg(x + static_cast<size_t>(e / K) * K + p) : static_cast<uint16_t>(0);
+  // stored interleaved inside each 8-block: x0 x4 x1 x5 x2 x6 x3 x7 (K % 32 == 0, so blocks do not straddle rows)
+  const int dst = (e & ~7) | ((e & 3) << 1) | ((e >> 2) & 1);
+  xp[static_cast<size_t>(l) * M * K + dst] =
+      ok ? __ldg(x + static_cast<size_t>(e / K) * K + p) : static_cast<uint16_t>(0);
 }
 
 __device__ __forceinline__ bool valid_width(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
@@ -405,7 +419,7 @@ __device__ __forceinline__ bool valid_width(int b) { return b == 2 || b == 3 || 
 // ---------------------------------------------------------------- the kernel
 // MT: 8-token blocks (1 for M <= 8, 2 for M <= 16).
 
-template <int FMT, int MT>
+template <int FMT, int MT, bool XP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -652,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int B = decltype(width)::value;
         for (int j = j0; j < j1; ++j, o += B) {
           uint32_t xb[MT][4];
-          x_pairs(xrow0 + 64 * j, xb[0]);
-          if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+          x_pairs<XP>(xrow0 + 64 * j, xb[0]);
+          if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
           if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
             qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
           else
@@ -676,8 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = static_cast<int>((widths >> (4 * j)) & 15u);
         if (b != 0) {  // 0: a segment the producer rejected (reported)
           uint32_t xb[MT][4];
-          x_pairs(xrow0 + 64 * j, xb[0]);
-          if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+          x_pairs<XP>(xrow0 + 64 * j, xb[0]);
+          if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
           if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
             qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
           else
@@ -709,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           scales4(sl + kSlotS + r * (kTN * 2) + col_off, s2);
         }
         uint32_t xb[MT][4];
-        x_pairs(xrow0 + 64 * j, xb[0]);
-        if constexpr (MT == 2) x_pairs(xrow1 + 64 * j, xb[MT - 1]);
+        x_pairs<XP>(xrow0 + 64 * j, xb[0]);
+        if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
         const uint4 wq = lds128(wrow + (4 * j + t) * kRowBytes);
         uint32_t P[4][4];
 #pragma unroll
@@ -796,18 +810,22 @@ namespace {
 
 using KernelFn = void (*)(GemvMaps, GemvArgs);
 
-template <int FMT>
+template <int FMT, bool XP>
 KernelFn pick_for(int M) {
-  return M <= 8 ? gemv_kernel<FMT, 1> : gemv_kernel<FMT, 2>;
+  return M <= 8 ? gemv_kernel<FMT, 1, XP> : gemv_kernel<FMT, 2, XP>;
 }
 
-KernelFn pick_kernel(int fmt, int M) {
-  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4>(M)
-         : fmt == EXQ_FMT_EXL2 ? pick_for<EXQ_FMT_EXL2>(M)
-                               : pick_for<EXQ_FMT_EXL2_QSCALE>(M);
+// XP: x comes from the gather kernel, pair-interleaved
+template <bool XP>
+KernelFn pick_fmt(int fmt, int M) {
+  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4, XP>(M)
+         : fmt == EXQ_FMT_EXL2 ? pick_for<EXQ_FMT_EXL2, XP>(M)
+                               : pick_for<EXQ_FMT_EXL2_QSCALE, XP>(M);
 }
 
-int variant_index(int fmt, int M) { return 2 * (fmt - 1) + (M <= 8 ? 0 : 1); }
+KernelFn pick_kernel(int fmt, int M, bool xp) { return xp ? pick_fmt<true>(fmt, M) : pick_fmt<false>(fmt, M); }
+
+int variant_index(int fmt, int M, bool xp) { return 4 * (fmt - 1) + 2 * (xp ? 1 : 0) + (M <= 8 ? 0 : 1); }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -865,7 +883,7 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
 }
 
 std::mutex g_attr_mutex;
-bool g_attr_done[64][6];
+bool g_attr_done[64][12];
 
 }  // namespace
 
@@ -890,10 +908,10 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
     return EXQ_ERR_INVALID_ARG;
   const exq_weight& w0 = w[0];
 
-  KernelFn fn = pick_kernel(w0.format, M);
+  KernelFn fn = pick_kernel(w0.format, M, plan.gather);
   {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    bool& done = g_attr_done[dev][variant_index(w0.format, M)];
+    bool& done = g_attr_done[dev][variant_index(w0.format, M, plan.gather)];
     if (!done) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess)
         return EXQ_ERR_CUDA;

@@ -295,13 +295,12 @@ __device__ __forceinline__ void exl2_unpack(const uint8_t* row, uint32_t off, ui
   }
 }
 
-// the lane's four scales of one scale row, each in both halves of a word
+// the lane's four scales of one scale row: s2[c] is the word holding column
+// c's scale, in its low half for even c and its high half for odd c
 __device__ __forceinline__ void scales4(const uint8_t* p, uint32_t (&s2)[4]) {
   const uint2 v = lds64(p);
-  s2[0] = prmt(v.x, v.x, 0x1010);
-  s2[1] = prmt(v.x, v.x, 0x3232);
-  s2[2] = prmt(v.y, v.y, 0x1010);
-  s2[3] = prmt(v.y, v.y, 0x3232);
+  s2[0] = s2[1] = v.x;
+  s2[2] = s2[3] = v.y;
 }
 
 // the same from two-level scales: `codes` = the lane's four 4-bit codes in
@@ -310,18 +309,31 @@ __device__ __forceinline__ void qscales4(uint32_t codes, const uint2& mv, uint32
   const uint32_t lo = codes & 0xFFFFu, hi = lo >> 8;
   const uint32_t a = two_level_scale2(lo | (lo << 12), mv.x);  // columns 0, 1
   const uint32_t b = two_level_scale2(hi | (hi << 12), mv.y);  // columns 2, 3
-  s2[0] = prmt(a, a, 0x1010);
-  s2[1] = prmt(a, a, 0x3232);
-  s2[2] = prmt(b, b, 0x1010);
-  s2[3] = prmt(b, b, 0x3232);
+  s2[0] = s2[1] = a;
+  s2[2] = s2[3] = b;
 }
 
-// w = fp16_RN((q - z) s) for the lane's four columns
+__device__ __forceinline__ __half2 as_h2(uint32_t v) {
+  __half2 h;
+  memcpy(&h, &v, 4);
+  return h;
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+  uint32_t v;
+  memcpy(&v, &h, 4);
+  return v;
+}
+
+// w = fp16_RN((q - z) s) for the lane's four columns: each pair times the
+// low or the high half of its scale word, broadcast (one fp16 multiply,
+// round to nearest even)
 __device__ __forceinline__ void scale_pairs(uint32_t (&P)[4][4], const uint32_t (&s2)[4]) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 4; ++c) {
+    const __half2 s = (c & 1) ? __high2half2(as_h2(s2[c])) : __low2half2(as_h2(s2[c]));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) P[c][i] = hmul2(P[c][i], s2[c]);
+    for (int i = 0; i < 4; ++i) P[c][i] = as_u32(__hmul2_rn(as_h2(P[c][i]), s));
+  }
 }
 
 // one EXL2 segment of width B, whole: unpack, scale, multiply (each width

@@ -676,6 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a stage of one width: the width is known for the whole run
       auto run = [&](auto width) {
         constexpr int B = decltype(width)::value;
+#pragma unroll 2
         for (int j = j0; j < j1; ++j, o += B) {
           uint32_t xb[MT][4];
           x_pairs<XP>(xrow0 + 64 * j, xb[0]);

@@ -1,4 +1,5 @@
-// Decode-sized fused quantized matmul, 1 <= M <= 16:  y = x . dequant(Wq).
+// Decode-sized fused quantized matmul, 1 <= M <= 16:  y = x . dequant(Wq),
+// for one layer or for up to four layers that read the same x in one launch.
 //
 // Follows the fused kernel of the ExLlamaV2 blog post ("ExLlamaV2: The fastest
 // inference engine for quantized Llama/HF models", section "How the Fused CUDA
@@ -9,7 +10,8 @@
 // weights stream in stored order.
 //
 // GB300 mapping:
-//  * Work is the list of (248-column tile, 32-row segment) units, tile-major.
+//  * Work is the list of (248-column tile, 32-row segment) units, tile-major,
+//    over all layers of the launch (their tiles numbered one after another).
 //    Every CTA (one per SM) takes an equal contiguous share, so all SMs
 //    stream the same number of bytes whatever N and K are. A share falls into
 //    pieces, one per tile it touches.
@@ -34,14 +36,17 @@
 //    off exactly in fp16 and each pair is scaled once (w = fp16_RN((q - z) s),
 //    the definition: the result is x times the rounded fp16 weights), then
 //    fed to mma.sync m16n8k16 (fp16 in, fp32 accumulate) as the A operand of a
-//    swapped product (A = W^T, B = x^T).
+//    swapped product (A = W^T, B = x^T). A stage whose EXL2 segments share one
+//    width runs a loop compiled for that width (one dispatch per stage).
 //  * At the end of a piece each warp writes fp32 partial sums of its 32
 //    columns and K group to the caller's workspace; the warp that arrives
 //    last at its (tile, column group) counter adds the tile's partials in
 //    piece order, writes y and puts the counter back to zero. Deterministic,
 //    and no warp ever waits on another CTA.
 //  * An act-order layer's x is gathered into stored-row order by a small
-//    kernel first (into the workspace), once per call rather than per CTA.
+//    kernel first (into the workspace), once per call rather than per CTA; it
+//    stores each 8-block as x0 x4 x1 x5 x2 x6 x3 x7, so that the consumers
+//    read the MMA's operand pairs directly.
 //  * EXL2 with two-level scales: instead of the scale box, the stage's rows
 //    of 4-bit scale codes follow as 4-byte asynchronous copies (like GPTQ
 //    zeros) and the tile's fp16 column maxima as one 16-byte copy per lane;

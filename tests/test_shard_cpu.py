@@ -73,3 +73,24 @@ def test_shard_reductions_exl2():
     y = x @ W
     assert np.array_equal(np.concatenate([x @ W[:, :16], x @ W[:, 16:]], axis=1), y)
     assert np.allclose(x[:, :96] @ W[:96] + x[:, 96:] @ W[96:], y, rtol=1e-12, atol=1e-12)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the --impl reference arm (the CPU oracle) runs on any host: one JSON line
+    # with the fields the harness reads, its e2e moving no host-device bytes
+    import json
+    import subprocess
+    import sys
+    from pathlib import Path
+
+    root = Path(__file__).resolve().parents[1]
+    r = subprocess.run([sys.executable, str(root / "bench.py"), "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=root,
+                       env={**os.environ, "OMP_NUM_THREADS": "1"})
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 1 and line["warmup"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "decode_stream_70b_exl2_4p0bpw"

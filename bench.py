@@ -247,7 +247,9 @@ PREFILL_SHAPES = (("q", 8192, 8192), ("k", 8192, 1024), ("gate", 8192, 28672), (
 
 def run_prefill(args, device):
     """The prefill GEMM over the Llama-2-70B projection shapes at M = 512 and
-    2048, GPTQ g128 (no act-order) and EXL2 2.5 bpw from {2, 3, 4}; packed
+    2048, GPTQ g128 (no act-order) and EXL2 2.5 bpw from {2, 3, 4}; at M = 2048
+    also EXL2 with two-level scales, GPTQ with act-order and EXL2 with a row
+    permutation (x gathered first, inside the timed launch); packed
     words drawn uniformly on the device (the packing is a bijection, so this is
     the distribution of uniform codes). CUDA events around `--steps` launches
     after `--warmup`; TFLOPS = 2 M K N / time."""
@@ -265,8 +267,9 @@ def run_prefill(args, device):
     except Exception:
         peak_bf16 = 1900.0
     shapes = {}
-    for fmt in ("gptq_g128", "exl2_2.5bpw", "exl2_2.5bpw_two_level"):
-        for M in ((2048,) if fmt.endswith("two_level") else (512, 2048)):
+    for fmt in ("gptq_g128", "exl2_2.5bpw", "exl2_2.5bpw_two_level", "gptq_g128_act_order", "exl2_2.5bpw_permuted"):
+        variant = fmt.endswith(("two_level", "act_order", "permuted"))
+        for M in ((2048,) if variant else (512, 2048)):
             for name, K, N in PREFILL_SHAPES:
                 gen = torch.Generator(device=device)
                 gen.manual_seed(1000 * M + K + N)
@@ -276,11 +279,12 @@ def run_prefill(args, device):
                     qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
                                        generator=gen).to(torch.int32)
                     sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
-                    w = exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device)
+                    pm = torch.randperm(K, device=device, generator=gen).int() if fmt.endswith("act_order") else None
+                    w = exq.gptq_weight(qw, qz, sc, pm, K, N, 128, device=device)
                 else:
                     bits = synth.solve_bit_mix(K // 32, 2.5, (2, 3, 4), np.random.default_rng(K + N))
                     w = exl2_device_layer(exq, torch, K, N, bits, gen, device,
-                                          two_level=fmt.endswith("two_level"), perm=False)
+                                          two_level=fmt.endswith("two_level"), perm=fmt.endswith("permuted"))
                 x = torch.randn(M, K, device=device, generator=gen).half()
                 y = torch.empty(M, N, device=device, dtype=torch.float16)
                 nws = exq.exq_gemm_workspace_size(w, M)

@@ -251,7 +251,16 @@ __device__ __forceinline__ uint4 natural_order(const uint32_t (&P)[4]) {
   return o;
 }
 
-template <int B>
+// the same in the K order of the x tile: natural, or, when the gather stored
+// x pair-interleaved (XP: k0 k4 k1 k5 k2 k6 k3 k7), the unpackers' pairs as
+// they are
+template <bool XP>
+__device__ __forceinline__ uint4 k_order(const uint32_t (&P)[4]) {
+  if constexpr (XP) return make_uint4(P[0], P[1], P[2], P[3]);
+  return natural_order(P);
+}
+
+template <int B, bool XP>
 __device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col, uint32_t s2) {
   int wi, off;
   block_window(B, t, wi, off);
@@ -261,16 +270,16 @@ __device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col
   unpack8<B>(fshr(wa, wb, off), wb >> off, P);
 #pragma unroll
   for (int i = 0; i < 4; ++i) P[i] = hmul2(P[i], s2);
-  return natural_order(P);
+  return k_order<XP>(P);
 }
 
 // the 32 codes of one column of a width-B segment -> 16 registers of fp16
 // pairs in K order (one TMEM A-operand row of the half slab)
-template <int B>
+template <int B, bool XP>
 __device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint32_t (&r)[16]) {
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const uint4 o = exl2_block<B>(rows, t, col, s2);
+    const uint4 o = exl2_block<B, XP>(rows, t, col, s2);
     r[4 * t + 0] = o.x;
     r[4 * t + 1] = o.y;
     r[4 * t + 2] = o.z;
@@ -280,7 +289,7 @@ __device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint
 
 // ---------------------------------------------------------------- the kernel
 
-template <int FMT>
+template <int FMT, bool XP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           unpack8_gptq(packed[(4 * h + t) * BN + col], zlo, zhi, P);
 #pragma unroll
           for (int j = 0; j < 4; ++j) P[j] = hmul2(P[j], s2);
-          const uint4 o = natural_order(P);
+          const uint4 o = k_order<XP>(P);
           r[4 * t + 0] = o.x;
           r[4 * t + 1] = o.y;
           r[4 * t + 2] = o.z;
@@ -458,12 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
         // one branch per 32-row segment (warp-uniform), each width's 4 blocks unrolled inside
         switch (b) {
-          case 2: exl2_segment<2>(rows, col, s2, r); break;
-          case 3: exl2_segment<3>(rows, col, s2, r); break;
-          case 4: exl2_segment<4>(rows, col, s2, r); break;
-          case 5: exl2_segment<5>(rows, col, s2, r); break;
-          case 6: exl2_segment<6>(rows, col, s2, r); break;
-          case 8: exl2_segment<8>(rows, col, s2, r); break;
+          case 2: exl2_segment<2, XP>(rows, col, s2, r); break;
+          case 3: exl2_segment<3, XP>(rows, col, s2, r); break;
+          case 4: exl2_segment<4, XP>(rows, col, s2, r); break;
+          case 5: exl2_segment<5, XP>(rows, col, s2, r); break;
+          case 6: exl2_segment<6, XP>(rows, col, s2, r); break;
+          case 8: exl2_segment<8, XP>(rows, col, s2, r); break;
           default:
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = 0u;
@@ -541,7 +550,7 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restri
 // x_perm[m][j] = x[m][perm[j]]: act-order rows gathered once so the tensor map
 // reads activations in stored-row order
 __global__ void permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                 uint16_t* __restrict__ xp, int M, int K) {
+                                 uint16_t* __restrict__ xp, int M, int K, bool interleave) {
   const int chunks = K / 8;
   const long long total = static_cast<long long>(M) * chunks;
   for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
@@ -550,11 +559,14 @@ __global__ void permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* 
     const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c));
     const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c + 4));
     const uint16_t* xr = x + static_cast<size_t>(m) * K;
+    const uint32_t v0 = __ldg(xr + p0.x), v1 = __ldg(xr + p0.y), v2 = __ldg(xr + p0.z), v3 = __ldg(xr + p0.w);
+    const uint32_t v4 = __ldg(xr + p1.x), v5 = __ldg(xr + p1.y), v6 = __ldg(xr + p1.z), v7 = __ldg(xr + p1.w);
     uint4 o;
-    o.x = __ldg(xr + p0.x) | (static_cast<uint32_t>(__ldg(xr + p0.y)) << 16);
-    o.y = __ldg(xr + p0.z) | (static_cast<uint32_t>(__ldg(xr + p0.w)) << 16);
-    o.z = __ldg(xr + p1.x) | (static_cast<uint32_t>(__ldg(xr + p1.y)) << 16);
-    o.w = __ldg(xr + p1.z) | (static_cast<uint32_t>(__ldg(xr + p1.w)) << 16);
+    if (interleave) {  // k0 k4 k1 k5 k2 k6 k3 k7
+      o = make_uint4(v0 | (v4 << 16), v1 | (v5 << 16), v2 | (v6 << 16), v3 | (v7 << 16));
+    } else {
+      o = make_uint4(v0 | (v1 << 16), v2 | (v3 << 16), v4 | (v5 << 16), v6 | (v7 << 16));
+    }
     *reinterpret_cast<uint4*>(xp + static_cast<size_t>(m) * K + 8 * c) = o;
   }
 }
@@ -623,7 +635,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     uint16_t* xp = static_cast<uint16_t*>(workspace);
     const long long total = static_cast<long long>(M) * (w.K / 8);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4096));
-    permute_x_kernel<<<blocks, 256, 0, stream>>>(x, w.perm, xp, M, w.K);
+    permute_x_kernel<<<blocks, 256, 0, stream>>>(x, w.perm, xp, M, w.K, true);
     if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
     xa = xp;
   }
@@ -684,11 +696,14 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   args.split = plan.split;
   args.slabs_per = plan.slabs_per;
 
-  auto fn = w.format == EXQ_FMT_GPTQ4 ? gemm_kernel<EXQ_FMT_GPTQ4>
-            : w.format == EXQ_FMT_EXL2  ? gemm_kernel<EXQ_FMT_EXL2>
-                                        : gemm_kernel<EXQ_FMT_EXL2_QSCALE>;
-  static std::once_flag attr_once[3];
-  std::call_once(attr_once[w.format - 1],
+  // a permuted layer's x comes from the gather, pair-interleaved
+  const bool xp_mode = w.perm != nullptr;
+  auto fn = w.format == EXQ_FMT_GPTQ4 ? (xp_mode ? gemm_kernel<EXQ_FMT_GPTQ4, true> : gemm_kernel<EXQ_FMT_GPTQ4, false>)
+            : w.format == EXQ_FMT_EXL2
+                ? (xp_mode ? gemm_kernel<EXQ_FMT_EXL2, true> : gemm_kernel<EXQ_FMT_EXL2, false>)
+                : (xp_mode ? gemm_kernel<EXQ_FMT_EXL2_QSCALE, true> : gemm_kernel<EXQ_FMT_EXL2_QSCALE, false>);
+  static std::once_flag attr_once[6];
+  std::call_once(attr_once[2 * (w.format - 1) + (xp_mode ? 1 : 0)],
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
   {
     cudaLaunchConfig_t cfg{};

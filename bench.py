@@ -744,7 +744,7 @@ def run_exq(args, rank, world, device):
 
 # ----------------------------------------------------------------------------- oracle
 
-def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 8):
+def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 48):
     """Time the CPU oracle (as it stands) on a bounded sample of the stream:
     whole k / v projections (8192 x 1024) of the first layers, packed words
     drawn exactly as in the GPU stream's recipe (numpy side). Runs in this

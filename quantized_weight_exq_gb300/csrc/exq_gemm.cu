@@ -11,11 +11,12 @@
 // tokens and per 64-row K slab:
 //
 //   warp 0      TMA producer: the x tile (256 tokens x 64 fp16, 128-byte
-//               swizzle), the packed word rows of the slab (one tensor-map box
-//               of 8 rows x 128 columns for GPTQ; one box per 32-row EXL2
-//               segment, of exactly its width, from a tensor map per width),
-//               its scale rows and GPTQ zero rows, all completing on one
-//               mbarrier per stage (5 stages).
+//               swizzle), the packed word rows of the slab as one tensor-map
+//               box of 128 columns (8 rows for GPTQ; 16 rows for EXL2, the
+//               most two segments take, so the box may run into the next
+//               slab's rows: one copy per slab costs less than one per
+//               segment), its scale rows and GPTQ zero rows, all completing
+//               on one mbarrier per stage (5 stages).
 //   warps 2-9   dequantisers: thread = output column (its TMEM lane), warp
 //               pair = the slab's two 32-row halves; packed words -> exact
 //               fp16 (q - z) -> * s, stored with tcgen05.st as the K-major A
@@ -57,6 +58,7 @@ constexpr int kThreads = (2 + kDequantWarps) * 32;
 // per-stage shared memory layout (bytes)
 constexpr int kXBytes = BT * BK * 2;        // 32 KB, 1024-aligned
 constexpr int kPackedBytes = 16 * BN * 4;   // up to 16 word rows (two 8-bit segments)
+__host__ __device__ constexpr int packed_rows(int fmt) { return fmt == EXQ_FMT_GPTQ4 ? 8 : 16; }
 constexpr int kScaleBytes = 2 * BN * 2;     // two 32-row halves
 constexpr int kZeroStride = 128;            // each half's zero row on its own 128-byte boundary (TMA)
 constexpr int kZeroBytes = 2 * kZeroStride;
@@ -89,14 +91,12 @@ constexpr int kMinSlabsPerSplit = 8;
 constexpr int kSplitSmBound = 256;  // SM count the workspace bound allows for
 
 struct GemmMaps {
-  CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 128, 128-byte swizzle
-  CUtensorMap w[6];  // qweight [rows, N] uint32, boxes 256 columns x b rows, b in {2,3,4,5,6,8}
+  CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 256, 128-byte swizzle
+  CUtensorMap w;     // qweight [rows, N] uint32, boxes 128 columns x 8 (GPTQ) or 16 (EXL2) rows
   CUtensorMap s;     // scales [groups, N] fp16, boxes 128 x 1 (unused with two-level scales)
   CUtensorMap z;     // GPTQ zeros or two-level scale codes [groups, N / 8] uint32, boxes 16 x 1
 };
 
-// tensor map of a box of b word rows
-__device__ __forceinline__ int wmap_index(int b) { return b == 8 ? 5 : b - 2; }
 
 struct GemmArgs {
   const uint32_t* seg_off;
@@ -367,18 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[s].rows1 = rows1;
         const int rows = rows0 + rows1;
         // boxes always move their full size (rows past M and columns past N read as zero)
-        uint32_t tx = kXBytes + static_cast<uint32_t>(rows) * BN * 4u;
+        uint32_t tx = kXBytes + (rows > 0 ? static_cast<uint32_t>(packed_rows(FMT)) * BN * 4u : 0u);
         if constexpr (FMT != EXQ_FMT_EXL2_QSCALE) tx += 2u * BN * 2u;  // fp16 scale rows
         if constexpr (FMT != EXQ_FMT_EXL2) tx += 2u * (BN / 8) * 4u;   // zero or scale-code rows
         mbar_expect_tx(bar, tx);
         tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
-        if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(8)], n0, row_start, bar);
-        } else if (rows > 0) {
-          tma_load_2d(smem_u32(st + kOffPacked), &maps.w[wmap_index(rows0)], n0, row_start, bar);
-          tma_load_2d(smem_u32(st + kOffPacked + rows0 * BN * 4), &maps.w[wmap_index(rows1)], n0, row_start + rows0,
-                      bar);
-        }
+        if (rows > 0) tma_load_2d(smem_u32(st + kOffPacked), &maps.w, n0, row_start, bar);
         for (int h = 0; h < 2; ++h) {
           const int g = FMT == EXQ_FMT_GPTQ4 ? (kt * BK + 32 * h) / a.gs : 2 * kt + h;
           if constexpr (FMT != EXQ_FMT_EXL2_QSCALE)
@@ -652,13 +646,11 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return EXQ_ERR_CUDA;
   }
-  static const int kWidths[6] = {2, 3, 4, 5, 6, 8};
-  for (int i = 0; i < 6; ++i) {
-    if (w.format == EXQ_FMT_GPTQ4 && kWidths[i] != 8) continue;  // GPTQ: 8 word rows per 64-row slab
+  {
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_word_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 4};
-    const cuuint32_t box[2] = {BN, static_cast<cuuint32_t>(kWidths[i])};
-    if (enc(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qweight), gdim, gstride, box, es,
+    const cuuint32_t box[2] = {BN, static_cast<cuuint32_t>(packed_rows(w.format))};
+    if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qweight), gdim, gstride, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return EXQ_ERR_CUDA;

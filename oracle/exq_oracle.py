@@ -29,7 +29,7 @@ Sources (the ExLlamaV2 pages):
   2, 3, 4, 5, 6 and 8-bit codes may be mixed inside one linear layer, and the
   same row-remapping used for act-order GPTQ models carries the mix.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
 * Packed weights are [K/8, N] (GPTQ) or [sum(bits), N] (EXL2) uint32 words,
   N contiguous; packing runs along K, least-significant bits first.
 * EXL2 segment = 32 consecutive stored rows at one bit width b. For each

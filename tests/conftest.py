@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # tests marked gpu are skipped (not failed) when no GPU is visible, so the
-    # CPU suite stays green; on a GPU machine they run and must pass.
+    # CPU suite stays green; on a machine with a GPU they run and must pass.
     try:
         import torch
         has_gpu = torch.cuda.is_available()

@@ -639,3 +639,20 @@ def test_solve_exl2_bits_on_measured_errors():
     bits = O.solve_exl2_bits(err, 4 * 16)
     assert int(bits.astype(int).sum()) == 64 and set(bits.tolist()) <= set(O.EXL2_BITS)
     assert bits[2] == bits.max() and bits[2] > 4
+
+
+def test_exl2_segment_word_offsets_closed_form():
+    # a segment of width b packs 32 codes of b bits = b words, so segment s
+    # starts at the sum of the widths before it (worked by hand)
+    off = O.exl2_seg_word_off([2, 3, 8, 4, 5, 6])
+    assert off.dtype == np.uint32
+    assert off.tolist() == [0, 2, 5, 13, 17, 22, 28]
+    # and it agrees with the packer's own table on a drawn layer
+    rng = np.random.default_rng(5)
+    bits = rng.choice(O.EXL2_BITS, size=6)
+    K, N = 32 * bits.size, 16
+    q = np.stack([rng.integers(0, 1 << int(b), size=(32, N)) for b in bits]).reshape(K, N).astype(np.uint8)
+    s = np.full((bits.size, N), 0.01, dtype=np.float16)
+    qw, off_p = O.pack_exl2(q, bits, s, None)[:2]
+    assert np.array_equal(off_p, O.exl2_seg_word_off(bits))
+    assert qw.shape == (int(bits.sum()), N)

@@ -45,9 +45,11 @@ Readings where the pages are silent:
   Kernel Works"): a 4-bit code c per (segment, column), packed 8 per uint32
   along N (nibble i of word k = column 8k + i), and one fp16 maximum m per
   column. The pages do not say how a code maps to a fraction; the reading
-  here is (c + 1) / 16, so c = 15 is the maximum. The segment's fp16 scale is
-  s = fp16_RNE(((c + 1) / 16) * m) (one rounding: the product is exact), and
-  the weight is then w = fp16_RNE((q - z) * s) as for fp16 scales.
+  here is (c + 1) / 16, so c = 15 is the maximum. The pages multiply
+  (w - 8) * scale * scale_max in float, where the product is exact (at most
+  8 + 5 + 11 significant bits), so the segment's scale s = ((c + 1) / 16) * m
+  is kept exact, never rounded to fp16 on its own, and the weight is
+  w = fp16_RNE((q - z) * s): one rounding, as for fp16 scales.
 * Dequantised weight w = fp16_RNE((q - z) * s): the product is exact in
   float32 and float64 (at most 8 + 11 significant bits), so there is exactly
   one rounding.
@@ -408,24 +410,34 @@ def unpack_exl2_qscale(words, N: int) -> np.ndarray:
 
 
 def exl2_two_level_scales(codes, scale_max) -> np.ndarray:
-    """fp16 bits [S, N] of s(g, n) = fp16_RNE(((c(g, n) + 1) / 16) * m(n)).
+    """Exact float64 values [S, N] of s(g, n) = ((c(g, n) + 1) / 16) * m(n).
 
-    codes uint8 [S, N] (0..15), scale_max fp16 [N]. The float64 product is
-    exact, so this is the single rounding of the definition."""
+    codes uint8 [S, N] (0..15), scale_max fp16 [N]. Not rounded: the
+    product has at most 5 + 11 significant bits, so float64 holds it."""
     c = np.asarray(codes, dtype=np.int64)
     m = _as_f64(scale_max)
     frac = (c + 1).astype(np.float64) / 16.0        # exact: k / 16, k = 1..16
-    return fp16_bits_from_float64(frac * m[None, :])
+    return frac * m[None, :]
 
 
 def dequant_exl2_qscale(qweight, seg_word_off, bits, q_scale, scale_max, perm, cols=None) -> np.ndarray:
     """fp16 bits of W [K, N'] in ORIGINAL row order from packed EXL2 with
-    two-level scales: the segment scales of exl2_two_level_scales, then the
-    fp16-scale definition of dequant_exl2."""
+    two-level scales: w(j, n) = fp16_RNE((q(j, n) - 2^(b-1)) * s(j // 32, n))
+    with the exact scales of exl2_two_level_scales (one rounding: the float64
+    product is exact), then W[perm[j]] = w(j)."""
     q_scale = np.asarray(q_scale, dtype=np.uint32)
     N = q_scale.shape[1] * 8
+    bits = np.asarray(bits, dtype=np.int64)
     s = exl2_two_level_scales(unpack_exl2_qscale(q_scale, N), scale_max)
-    return dequant_exl2(qweight, seg_word_off, bits, s, perm, cols=cols)
+    if cols is not None:
+        cols = np.asarray(cols, dtype=np.int64)
+        qweight = np.asarray(qweight, dtype=np.uint32)[:, cols]
+        s = s[:, cols]
+    q = unpack_exl2_codes(qweight, bits, seg_word_off).astype(np.int64)
+    seg = np.arange(q.shape[0]) // SEGMENT_ROWS
+    z = (np.int64(1) << (bits[seg] - 1))[:, None]
+    w = (q - z).astype(np.float64) * s[seg]
+    return _scatter_rows(fp16_bits_from_float64(w), perm)
 
 
 # ----------------------------------------------------------------------------

@@ -427,27 +427,52 @@ def test_bit_mix_is_exact():
 
 # ---------------------------------------------------------------- EXL2 two-level scales
 
+def _qscale_weight(m_bits: int, c: int, v: int) -> int:
+    """The oracle's dequantised weight for one (m, c, v = q - 128) through a
+    one-segment, eight-column EXL2 layer of width 8 (packed by the oracle)."""
+    q = np.full((32, 8), 128, dtype=np.uint8)
+    q[0, 0] = v + 128
+    bits = np.array([8])
+    qw, off, _, _ = O.pack_exl2(q, bits, np.ones((1, 8), np.float16), None)
+    codes = np.zeros((1, 8), np.uint8)
+    codes[0, 0] = c
+    m = np.full(8, m_bits, dtype=np.uint16)
+    return int(O.dequant_exl2_qscale(qw, off, bits, O.pack_exl2_qscale(codes), m, None)[0, 0])
+
+
 def test_exl2_qscale_golden():
-    # hand-derived effective scales, including ties, subnormals and the largest finite value
+    # hand-derived weights, including cases where rounding the scale to fp16
+    # first would give another weight, ties, subnormals, -0 and overflow
     for row in _fixture("exl2_qscale.txt"):
-        m_hex, c, want = row.split()
-        m = np.array([int(m_hex, 16)], dtype=np.uint16)
-        got = int(O.exl2_two_level_scales(np.array([[int(c)]], np.uint8), m)[0, 0])
-        assert got == int(want, 16), (m_hex, c, hex(got), want)
+        m_hex, c, v, want = row.split()
+        got = _qscale_weight(int(m_hex, 16), int(c), int(v))
+        assert got == int(want, 16), (m_hex, c, v, hex(got), want)
 
 
 def test_exl2_qscale_matches_exact_rational_rounding():
-    # every code against every fp16 maximum of a few binades (normal and
-    # subnormal, both signs): the exact rational (c + 1) / 16 * m rounded by
-    # Python's own binary16 conversion (struct 'e')
-    hs = np.concatenate([np.arange(0x0000, 0x0800, 7), np.arange(0x2C00, 0x3C00, 13), np.arange(0x7800, 0x7C00, 11),
-                         np.arange(0x8001, 0x8400, 17)]).astype(np.uint16)
-    codes = np.arange(16, dtype=np.uint8)[:, None].repeat(hs.size, axis=1)
-    got = O.exl2_two_level_scales(codes, hs)
-    mv = O.float64_from_fp16_bits(hs)
+    # every code, several values of q - z, against every fp16 maximum of a few
+    # binades (normal and subnormal, both signs): the exact rational
+    # v * (c + 1) / 16 * m rounded once by Python's own binary16 conversion
+    # (struct 'e'; the float64 it starts from holds the rational exactly)
+    hs = np.concatenate([np.arange(0x0000, 0x0800, 37), np.arange(0x2C00, 0x3C00, 53), np.arange(0x5000, 0x5800, 41),
+                         np.arange(0x8001, 0x8400, 67)]).astype(np.uint16)
+    vs = np.array([-128, -77, -8, -3, -1, 0, 1, 3, 7, 13, 31, 127])
+    q = np.zeros((32, hs.size), dtype=np.uint8)
     for c in range(16):
-        want = [_py_half_bits(float(Fraction(c + 1, 16) * Fraction(float(v)))) for v in mv]
-        assert np.array_equal(got[c], np.array(want, dtype=np.uint16)), c
+        for i, v in enumerate(vs):
+            q[i] = v + 128
+        qw, off, _, _ = O.pack_exl2(q, np.array([8]), np.ones((1, hs.size), np.float16), None)
+        codes = np.full((1, hs.size), c, np.uint8)
+        pad = (-hs.size) % 8
+        codes_p = np.pad(codes, ((0, 0), (0, pad)))
+        W = O.dequant_exl2_qscale(np.pad(qw, ((0, 0), (0, pad))), off, np.array([8]), O.pack_exl2_qscale(codes_p),
+                                  np.pad(hs, (0, pad)), None)[:, :hs.size]
+        mv = O.float64_from_fp16_bits(hs)
+        for i, v in enumerate(vs):
+            # the rational's value; a zero takes the IEEE sign of the float product
+            want = [_py_half_bits(float(Fraction(int(v)) * Fraction(c + 1, 16) * Fraction(float(x))) or
+                                  float(v) * float(x)) for x in mv]
+            assert np.array_equal(W[i], np.array(want, dtype=np.uint16)), (c, v)
 
 
 def test_exl2_qscale_packing():
@@ -469,18 +494,22 @@ def test_exl2_qscale_packing():
 
 
 def test_exl2_qscale_dequant_reduces_to_fp16_scales():
-    # with the effective scales rounded by numpy, the two-level format is the
-    # fp16-scale format; with every code 15 the scale is the column maximum
+    # where ((c + 1) / 16) * m is itself an fp16 value the two-level format is
+    # the fp16-scale format with that scale: every code 15 (the scale is the
+    # column maximum), and maxima with at most 7 significant bits (any code)
     inp = synth.exl2_layer(256, 48, bpw=4.0, seed=8)
     codes, m = synth.exl2_qscale_draws(8, 48, seed=8)
     qw, off, _, perm = O.pack_exl2(inp.q, inp.bits, inp.s, inp.perm)
     qs = O.pack_exl2_qscale(codes)
-    s_np = (m.astype(np.float64)[None, :] * (codes.astype(np.float64) + 1) / 16).astype(np.float16)
     W = O.dequant_exl2_qscale(qw, off, inp.bits, qs, m, perm)
-    assert np.array_equal(W, O.dequant_exl2_definitional(inp.q, inp.bits, s_np, inp.perm))
     top = O.pack_exl2_qscale(np.full((8, 48), 15, np.uint8))
     W_top = O.dequant_exl2_qscale(qw, off, inp.bits, top, m, perm)
     assert np.array_equal(W_top, O.dequant_exl2_definitional(inp.q, inp.bits, np.tile(m, (8, 1)), inp.perm))
+    m7 = (m.view(np.uint16) & np.uint16(0xFFF0)).view(np.float16)   # 7 significant bits
+    s7 = (m7.astype(np.float64)[None, :] * (codes.astype(np.float64) + 1) / 16).astype(np.float16)
+    assert np.array_equal(s7.astype(np.float64), m7.astype(np.float64)[None, :] * (codes + 1) / 16)  # exact
+    W7 = O.dequant_exl2_qscale(qw, off, inp.bits, qs, m7, perm)
+    assert np.array_equal(W7, O.dequant_exl2_definitional(inp.q, inp.bits, s7, inp.perm))
     cols = np.array([0, 9, 47])
     assert np.array_equal(O.dequant_exl2_qscale(qw, off, inp.bits, qs, m, perm, cols=cols), W[:, cols])
 

@@ -59,6 +59,9 @@
  *  - Kernels that wait on on-chip barriers give up after a bounded time,
  *    record EXQ_ERR_TIMEOUT in the device error word and return; read it with
  *    exq_get_last_device_error().
+ *  - Per-device set-up (kernel attributes, exq_gemm_noalloc's scratch
+ *    address) is done on the first call on a device and kept; after
+ *    cudaDeviceReset the process must not use the library on that device.
  *  - Device pointers must be 16-byte aligned; N % 8 == 0; GPTQ needs
  *    K % group_size == 0 and group_size % 32 == 0; EXL2 needs K % 32 == 0.
  *  - fp16 values travel as their uint16 bit patterns.
@@ -147,6 +150,19 @@ exq_status exq_pack_exl2_qscale(const uint8_t* codes, int32_t S, int32_t N, uint
  * Returns -1 if bits is NULL, n_segments <= 0 or a width is outside the set. */
 int64_t exq_exl2_word_rows(const uint8_t* bits, int32_t n_segments);
 
+/* exq_exl2_seg_word_off -- host-only, synchronous, no CUDA.
+ * The segment table of an EXL2 layer (the row remapping of the ExLlamaV2
+ * README, "EXL2 quantization", stores each segment's words after the previous
+ * one's): seg_word_off_out[s] = bits[0] + ... + bits[s-1] for s = 0..S, so
+ * segment s occupies word rows [seg_word_off_out[s], seg_word_off_out[s+1]).
+ *   bits  [S] widths in {2,3,4,5,6,8} (host)
+ *   seg_word_off_out [S + 1] uint32 (host, caller-allocated)
+ * exq_pack_exl2 writes the same table; this call serves callers that lay
+ * out the words themselves (exq_quantize_exl2 takes the table as input).
+ * Returns EXQ_ERR_INVALID_ARG for NULL buffers, S <= 0 or a width outside
+ * the set. */
+exq_status exq_exl2_seg_word_off(const uint8_t* bits, int32_t n_segments, uint32_t* seg_word_off_out);
+
 /* ---------------------------------------------------------------- device ops */
 
 /* exq_dequant -- W_out[perm[j]][n] = w(j, n) for every stored row j, i.e. the
@@ -174,7 +190,10 @@ size_t exq_gemv_workspace_size(const exq_weight* w, int32_t M);
  *              serves any sequence of calls (any layer, any M) ordered on one
  *              stream. The rest is scratch (partial sums and, for a permuted
  *              layer, x gathered into stored-row order). Calls that may
- *              overlap on the GPU need separate workspaces.
+ *              overlap on the GPU need separate workspaces. A call that ends
+ *              in EXQ_ERR_TIMEOUT (exq_get_last_device_error) may leave
+ *              counters non-zero: zero-fill the first 64 KB again before the
+ *              workspace serves another call.
  * Deterministic: the same inputs give the same bits.
  * Returns EXQ_ERR_UNSUPPORTED for M > 16 (use exq_gemm) and
  * EXQ_ERR_INVALID_ARG for a missing, short or misaligned workspace. */
@@ -226,7 +245,12 @@ exq_status exq_gemv_multi(const exq_weight* w, int32_t n, const uint16_t* x, int
  * current device. */
 size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M);
 
-/* exq_gemm -- prefill-sized fused matmul for any M >= 1 (tuned for M >= 128):
+/* exq_gemm -- prefill-sized fused matmul for any M >= 1 (tuned for M >= 128).
+ * The ExLlamaV2 blog post ("How the Fused CUDA Kernel Works", the paragraph
+ * after the conceptual kernel) says the real kernel handles several widths
+ * and uses tensor cores while keeping the same fused shape: packed weights
+ * are loaded, dequantized on the fly and multiplied, with no dense weight
+ * written to memory. Here that is
  * computed as y^T = W^T x^T on the tcgen05 tensor cores, the packed weights
  * dequantized to fp16 straight into tensor memory as the A operand, x read
  * by TMA as the B operand, fp32 accumulation in tensor memory.
@@ -257,9 +281,14 @@ exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t*
  *   grids of few tiles run slower and may round differently in the last bit.
  *   Returns EXQ_ERR_UNSUPPORTED (and launches nothing) if the layer has a
  *   permutation and M * K * 2 > EXQ_NOALLOC_SCRATCH_BYTES.
- *   The first call on a device looks up the scratch array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture. Nothing is allocated, then or later.
+ *   The array is part of the library's GEMM module, so the CUDA driver
+ *   commits it when that module loads on a device: with lazy module loading
+ *   (CUDA's default) that is during the first exq_gemm or exq_gemm_noalloc
+ *   call there. The first exq_gemm_noalloc call on a device, with or without
+ *   a permutation, also looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current). So make one call on
+ *   each device before any stream capture. The call itself allocates
+ *   nothing, then or later.
  *   Every call on a device shares the one array, which keeps the previous
  *   call's contents (the array is fully rewritten before it is read, so
  *   nothing needs clearing). Calls whose kernels overlap on the GPU (other

@@ -39,7 +39,7 @@ def _compile(src: str, verbose: bool) -> tuple[str, str]:
     s = CSRC / src
     if obj.exists() and obj.stat().st_mtime >= max(
             s.stat().st_mtime, *(p.stat().st_mtime for p in CSRC.glob("*.cuh")),
-            *(p.stat().st_mtime for p in CSRC.glob("*.h")), (ROOT / "include" / "exq.h").stat().st_mtime):
+            *(p.stat().st_mtime for p in CSRC.glob("*.h")), *(p.stat().st_mtime for p in (ROOT / "include").glob("*.h"))):
         return str(obj), ""
     cmd = [nvcc(), "-c", str(s), "-o", str(obj)] + _flags(src)
     if verbose and src.endswith(".cu"):

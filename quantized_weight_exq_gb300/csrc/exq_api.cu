@@ -1,9 +1,11 @@
 // Host entry points of libexq: argument checks, dispatch, status codes.
 // Every check here runs before any launch and has no side effects.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
 #include "exq_internal.h"
+#include "exq_testing.h"
 
 namespace exq {
 
@@ -50,6 +52,12 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uin
              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
+std::atomic<int> g_starve_rounds{0};
+}  // namespace
+
+int testing_starve_rounds() { return g_starve_rounds.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -261,4 +269,8 @@ extern "C" exq_status exq_get_last_device_error(void* stream) {
   if (v & kDevErrTimeout) return EXQ_ERR_TIMEOUT;
   if (v & (kDevErrBadSegment | kDevErrBadPerm)) return EXQ_ERR_INVALID_ARG;
   return EXQ_OK;
+}
+
+extern "C" void exq_testing_starve(int32_t wait_rounds) {
+  g_starve_rounds.store(wait_rounds > 0 ? wait_rounds : 0, std::memory_order_relaxed);
 }

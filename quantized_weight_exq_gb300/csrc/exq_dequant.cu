@@ -51,15 +51,20 @@ __device__ __forceinline__ uint32_t comp8(const uint4& a, const uint4& b, int c)
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <int B>
+// QS: two-level scales, s2 = the exact fractions (c + 1) / 16 and m2 the
+// column maxima (the first multiply is exact, the second is the rounding)
+template <int B, bool QS>
 __device__ __forceinline__ void exl2_block(const uint4 (&wa)[2], const uint4 (&wb)[2], int off,
-                                           const uint32_t (&s2)[8], uint32_t (&P)[8][4]) {
+                                           const uint32_t (&s2)[8], const uint32_t (&m2)[8], uint32_t (&P)[8][4]) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint32_t a = comp8(wa[0], wa[1], c), b = comp8(wb[0], wb[1], c);
     unpack8<B>(fshr(a, b, off), b >> off, P[c]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) P[c][i] = hmul2(P[c][i], s2[c]);
+    for (int i = 0; i < 4; ++i) {
+      P[c][i] = hmul2(P[c][i], s2[c]);
+      if constexpr (QS) P[c][i] = hmul2(P[c][i], m2[c]);
+    }
   }
 }
 
@@ -72,8 +77,8 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const __grid_constant
   if (s >= a.n_steps || col >= a.N) return;
 
   uint32_t P[8][4];
-  uint32_t s2[8];
-  uint4 sv;
+  uint32_t s2[8], m2[8];
+  uint4 sv, mv;
   if constexpr (FMT == EXQ_FMT_GPTQ4) {
     const int grp = s / a.gs_steps;
     const uint4 w0 = ld_stream(a.qweight + static_cast<size_t>(4 * s + t) * a.N + col);
@@ -109,28 +114,31 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const __grid_constant
       }
     }
     if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
-      // the 8 columns' codes are one word; their maxima one 16-byte vector
+      // the 8 columns' codes are one word (-> exact fractions); their maxima one 16-byte vector
       const uint32_t cw = __ldg(a.q_scale + static_cast<size_t>(s) * (a.N >> 3) + (col >> 3));
-      const uint4 mv = __ldg(reinterpret_cast<const uint4*>(a.q_scale_max + col));
-      sv.x = two_level_scale2((cw & 0xFFu) | ((cw & 0xF0u) << 12), mv.x);
-      sv.y = two_level_scale2(((cw >> 8) & 0xFFu) | ((cw & 0xF000u) << 4), mv.y);
-      sv.z = two_level_scale2(((cw >> 16) & 0xFFu) | ((cw >> 4) & 0xF0000u), mv.z);
-      sv.w = two_level_scale2((cw >> 24) | ((cw >> 12) & 0xF0000u), mv.w);
+      mv = __ldg(reinterpret_cast<const uint4*>(a.q_scale_max + col));
+      sv.x = two_level_frac2((cw & 0xFFu) | ((cw & 0xF0u) << 12));
+      sv.y = two_level_frac2(((cw >> 8) & 0xFFu) | ((cw & 0xF000u) << 4));
+      sv.z = two_level_frac2(((cw >> 16) & 0xFFu) | ((cw >> 4) & 0xF0000u));
+      sv.w = two_level_frac2((cw >> 24) | ((cw >> 12) & 0xF0000u));
     } else {
       sv = __ldg(reinterpret_cast<const uint4*>(a.scales + static_cast<size_t>(s) * a.N + col));
+      mv = sv;
     }
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint32_t h = comp8(sv, sv, c >> 1);
+      const uint32_t h = comp8(sv, sv, c >> 1), hm = comp8(mv, mv, c >> 1);
       s2[c] = (c & 1) ? prmt(h, h, 0x3232) : prmt(h, h, 0x1010);
+      m2[c] = (c & 1) ? prmt(hm, hm, 0x3232) : prmt(hm, hm, 0x1010);
     }
+    constexpr bool QS = FMT == EXQ_FMT_EXL2_QSCALE;
     switch (ok ? b : 0) {
-      case 2: exl2_block<2>(wa, wb, off, s2, P); break;
-      case 3: exl2_block<3>(wa, wb, off, s2, P); break;
-      case 4: exl2_block<4>(wa, wb, off, s2, P); break;
-      case 5: exl2_block<5>(wa, wb, off, s2, P); break;
-      case 6: exl2_block<6>(wa, wb, off, s2, P); break;
-      case 8: exl2_block<8>(wa, wb, off, s2, P); break;
+      case 2: exl2_block<2, QS>(wa, wb, off, s2, m2, P); break;
+      case 3: exl2_block<3, QS>(wa, wb, off, s2, m2, P); break;
+      case 4: exl2_block<4, QS>(wa, wb, off, s2, m2, P); break;
+      case 5: exl2_block<5, QS>(wa, wb, off, s2, m2, P); break;
+      case 6: exl2_block<6, QS>(wa, wb, off, s2, m2, P); break;
+      case 8: exl2_block<8, QS>(wa, wb, off, s2, m2, P); break;
       default:
         atomicOr(&g_dequant_err, kDevErrBadSegment);
 #pragma unroll

@@ -171,18 +171,20 @@ __device__ __forceinline__ void gptq_zero_consts(uint32_t z, uint32_t& zlo, uint
 }
 
 // EXL2 two-level scales, two columns at once: the codes c_lo and c_hi sit in
-// bits 0..3 and 16..19 of cc (other bits are ignored), m2 = (m_lo, m_hi) the
-// columns' fp16 maxima. Returns (s_lo, s_hi), s = fp16_RN(((c + 1) / 16) m):
-// (1024 + c) / 16 - 1023 / 16 = (c + 1) / 16 comes out exact from one fp16
-// fma, and the multiply by m is the one rounding.
+// bits 0..3 and 16..19 of cc (other bits are ignored). Returns the exact
+// fractions ((c_lo + 1) / 16, (c_hi + 1) / 16): (1024 + c) / 16 - 1023 / 16
+// comes out exact from one fp16 fma. The weight is then
+// fp16_RN(fp16_RN((q - z) * f) * m): the inner product (q - z) (c + 1) / 16
+// has at most 7 + 4 significant bits and lies in [1/16, 128] (or is 0), so it
+// is exact, and the multiply by the column maximum m is the one rounding of
+// w = fp16_RN((q - z) * ((c + 1) / 16) * m).
 constexpr uint32_t kNeg1023Over16 = f16_bits(-1023) - (4u << 10);  // -63.9375: exponent lowered by 4
 static_assert(kNeg1023Over16 == 0xD3FE, "f16 -1023/16");
 
-__device__ __forceinline__ uint32_t two_level_scale2(uint32_t cc, uint32_t m2) {
+__device__ __forceinline__ uint32_t two_level_frac2(uint32_t cc) {
   constexpr uint32_t sixteenth = pack2(f16_pow2_neg(4), f16_pow2_neg(4));
   constexpr uint32_t bias = pack2(kNeg1023Over16, kNeg1023Over16);
-  const uint32_t f = hfma2(and_or(cc, 0x000F000Fu, kMagic), sixteenth, bias);
-  return hmul2(f, m2);
+  return hfma2(and_or(cc, 0x000F000Fu, kMagic), sixteenth, bias);
 }
 
 // x / s rounded to an integer as rint(fp32_RN(x / s)): the quotient comes

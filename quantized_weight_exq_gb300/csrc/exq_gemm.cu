@@ -83,7 +83,7 @@ constexpr uint32_t kTmemA = BT;
 constexpr uint32_t kAStageCols = BK / 2;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kTmemA + kStages * kAStageCols <= kTmemCols, "tensor memory budget");
-constexpr long long kWaitLimit = 1ll << 22;  // try_wait rounds before giving up
+constexpr int kWaitLimit = 1 << 22;  // try_wait rounds before giving up
 
 // K split of grids with few tiles: at most 8 splits, each of at least 8 slabs
 constexpr int kMaxSplit = 8;
@@ -106,6 +106,8 @@ struct GemmArgs {
   int M, N, K, gs, n_word_rows;
   int split;        // CTAs along K (gridDim.z)
   int slabs_per;    // 64-row slabs per split (the last split may have fewer)
+  int wait_limit;   // polling rounds of a bounded wait (kWaitLimit unless a test lowers it)
+  int starve;       // test hook: the producer issues nothing, so the other roles' waits run out
 };
 
 struct StageMeta {  // written by the producer before the stage's copies
@@ -143,8 +145,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // bounded wait; returns false (and records a timeout) if the phase never completes
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  for (long long i = 0; i < kWaitLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int limit) {
+  for (int i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
   }
@@ -156,9 +158,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait by a whole warp: lane 0 polls and broadcasts, so the loop
 // exits for all lanes in the same round and warp-collective instructions that
 // follow (tcgen05.ld/st.sync.aligned, __syncwarp) are reached convergently.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               int limit) {
   const bool leader = (threadIdx.x & 31) == 0;
-  for (long long i = 0; i < kWaitLimit; ++i) {
+  for (int i = 0; i < limit; ++i) {
     int state = 0;  // 1 = phase complete, 2 = another role gave up
     if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
     state = __shfl_sync(0xffffffffu, state, 0);
@@ -260,8 +263,10 @@ __device__ __forceinline__ uint4 k_order(const uint32_t (&P)[4]) {
   return natural_order(P);
 }
 
-template <int B, bool XP>
-__device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col, uint32_t s2) {
+// QS: two-level scales, s2 = the exact fraction (c + 1) / 16 and m2 the
+// column maximum (the first multiply is exact, the second is the rounding)
+template <int B, bool XP, bool QS>
+__device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col, uint32_t s2, uint32_t m2) {
   int wi, off;
   block_window(B, t, wi, off);
   const uint32_t wa = rows[wi * BN + col];
@@ -269,17 +274,21 @@ __device__ __forceinline__ uint4 exl2_block(const uint32_t* rows, int t, int col
   uint32_t P[4];
   unpack8<B>(fshr(wa, wb, off), wb >> off, P);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) P[i] = hmul2(P[i], s2);
+  for (int i = 0; i < 4; ++i) {
+    P[i] = hmul2(P[i], s2);
+    if constexpr (QS) P[i] = hmul2(P[i], m2);
+  }
   return k_order<XP>(P);
 }
 
 // the 32 codes of one column of a width-B segment -> 16 registers of fp16
 // pairs in K order (one TMEM A-operand row of the half slab)
-template <int B, bool XP>
-__device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint32_t (&r)[16]) {
+template <int B, bool XP, bool QS>
+__device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint32_t s2, uint32_t m2,
+                                             uint32_t (&r)[16]) {
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const uint4 o = exl2_block<B, XP>(rows, t, col, s2);
+    const uint4 o = exl2_block<B, XP, QS>(rows, t, col, s2, m2);
     r[4 * t + 0] = o.x;
     r[4 * t + 1] = o.y;
     r[4 * t + 2] = o.z;
@@ -336,14 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !a.starve) {  // test hook: a starved producer issues nothing
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
       int issued = 0;
       for (int i = 0; i < n_iter; ++i) {
         const int kt = kt0 + i;
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.wait_limit)) break;
         uint8_t* st = smem + s * kStageBytes;
         const uint32_t bar = smem_u32(&full[s]);
         int rows0, rows1;
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every issued stage's copies must land before the CTA may exit
       for (int i = max(0, issued - kStages); i < issued; ++i) {
         const uint32_t bar = smem_u32(&full[i % kStages]);
-        for (long long r = 0; r < kWaitLimit; ++r)
+        for (int r = 0; r < a.wait_limit; ++r)
           if (mbar_try_wait(bar, (i / kStages) & 1)) break;
       }
     }
@@ -396,8 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_iter; ++i) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag)) break;
-        if (!mbar_wait(smem_u32(&aready[s]), ph, abort_flag)) break;
+        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, a.wait_limit)) break;
+        if (!mbar_wait(smem_u32(&aready[s]), ph, abort_flag, a.wait_limit)) break;
         tc_fence_after();
         const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes + kOffX));
         const uint32_t a_tmem = tmem + kTmemA + s * kAStageCols;
@@ -423,17 +432,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_iter; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort_flag)) break;
-      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1, abort_flag)) break;  // A stage read by earlier MMAs
+      if (!mbar_wait_warp(smem_u32(&full[s]), ph, abort_flag, a.wait_limit)) break;
+      if (!mbar_wait_warp(smem_u32(&empty[s]), ph ^ 1, abort_flag, a.wait_limit)) break;  // A stage read by earlier MMAs
       tc_fence_after();
       const uint8_t* st = smem + s * kStageBytes;
       const uint32_t* packed = reinterpret_cast<const uint32_t*>(st + kOffPacked);
       uint32_t s2;
       if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
-        // s = fp16_RN(((c + 1) / 16) m) from the column's 4-bit code
+        // the exact fraction (c + 1) / 16 of the column's 4-bit code; m2 follows
         const uint32_t cw = reinterpret_cast<const uint32_t*>(st + kOffZero + h * kZeroStride)[col >> 3];
         const uint32_t c = (cw >> (4 * (col & 7))) & 0xFu;
-        s2 = two_level_scale2(c | (c << 16), m2);
+        s2 = two_level_frac2(c | (c << 16));
       } else {
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + kOffScale);
         const uint32_t s16 = sc[h * BN + col];
@@ -461,12 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* rows = packed + (h == 0 ? 0 : meta[s].rows0) * BN;
         // one branch per 32-row segment (warp-uniform), each width's 4 blocks unrolled inside
         switch (b) {
-          case 2: exl2_segment<2, XP>(rows, col, s2, r); break;
-          case 3: exl2_segment<3, XP>(rows, col, s2, r); break;
-          case 4: exl2_segment<4, XP>(rows, col, s2, r); break;
-          case 5: exl2_segment<5, XP>(rows, col, s2, r); break;
-          case 6: exl2_segment<6, XP>(rows, col, s2, r); break;
-          case 8: exl2_segment<8, XP>(rows, col, s2, r); break;
+          case 2: exl2_segment<2, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
+          case 3: exl2_segment<3, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
+          case 4: exl2_segment<4, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
+          case 5: exl2_segment<5, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
+          case 6: exl2_segment<6, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
+          case 8: exl2_segment<8, XP, FMT == EXQ_FMT_EXL2_QSCALE>(rows, col, s2, m2, r); break;
           default:
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = 0u;
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     // accumulator lane = output column, accumulator column = token; warp h
     // takes tokens [128 h, 128 h + 128) of its lane quarter
-    if (mbar_wait_warp(smem_u32(accum), 0, abort_flag)) {
+    if (mbar_wait_warp(smem_u32(accum), 0, abort_flag, a.wait_limit) && !*abort_flag) {
       tc_fence_after();
       const int n = n0 + col;
 #pragma unroll 1
@@ -687,6 +696,9 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
   args.n_word_rows = w.n_word_rows;
   args.split = plan.split;
   args.slabs_per = plan.slabs_per;
+  const int starve = testing_starve_rounds();
+  args.wait_limit = starve > 0 ? starve : kWaitLimit;
+  args.starve = starve > 0 ? 1 : 0;
 
   // a permuted layer's x comes from the gather, pair-interleaved
   const bool xp_mode = w.perm != nullptr;
@@ -733,19 +745,23 @@ namespace {
 // every GPU that loads the library holds it until the process exits.
 __device__ __align__(256) uint8_t g_noalloc_scratch[EXQ_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on `dev`, looked up once per device
-// with that device current (in host code the symbol is only a host-side
-// stand-in, never a device address). nullptr if the lookup failed.
+// Device address of g_noalloc_scratch on `dev`, looked up with that device
+// current (in host code the symbol is only a host-side stand-in, never a
+// device address) on the first call that succeeds, then kept. A failed
+// lookup is not kept: the next call tries again. nullptr if it failed.
 void* noalloc_scratch(int dev) {
   constexpr int kMaxDevices = 64;
+  static std::mutex mu;
   static void* ptr[kMaxDevices];
-  static std::once_flag once[kMaxDevices];
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::call_once(once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess) ptr[dev] = p;
-    else cudaGetLastError();
-  });
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess)
+      ptr[dev] = p;
+    else
+      cudaGetLastError();
+  }
   return ptr[dev];
 }
 
@@ -754,14 +770,13 @@ void* noalloc_scratch(int dev) {
 exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream) {
   const size_t need = gather_bytes(w, M);
   if (need > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
-  if (need) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
-    scratch = noalloc_scratch(dev);
-    if (!scratch) return EXQ_ERR_CUDA;
-  }
-  return launch_gemm(w, x, M, y, scratch, need, stream);
+  // the set-up runs on the device's first call whatever the layer, so that a
+  // caller who makes one call before stream capture has done it
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
+  void* scratch = noalloc_scratch(dev);
+  if (!scratch) return EXQ_ERR_CUDA;
+  return launch_gemm(w, x, M, y, need ? scratch : nullptr, need, stream);
 }
 
 unsigned take_gemm_errors(cudaStream_t stream) {

@@ -15,34 +15,38 @@
 //    Every CTA (one per SM) takes an equal contiguous share, so all SMs
 //    stream the same number of bytes whatever N and K are. A share falls into
 //    pieces, one per tile it touches.
-//  * Warp 16 is the producer. It cuts each piece into stages of at most eight
-//    segments (256 rows of K) and at most 32 packed word rows, and moves a
-//    stage with three tensor-map copies into one slot of a shared-memory ring:
-//    the word rows (a 32-row x 248-column box), the scale rows (an 8 x 248
-//    box) and the stage's activations (a 256 x M box); GPTQ zero rows follow
-//    as 4-byte asynchronous copies. All of it completes on the slot's "full"
+//  * Warp 16 is the producer. It cuts each piece into stages of at most 32
+//    packed word rows (EXL2: the longest run of whole segments that fits, at
+//    most 16; GPTQ: 8-segment blocks aligned to 256 rows) and moves a stage
+//    with tensor-map copies into one slot of a shared-memory ring: the word
+//    rows (a 32-row x 248-column box), the scale rows (a 16 x 248 box) and the
+//    stage's activations (one or two 256 x M boxes); GPTQ zero rows follow as
+//    4-byte asynchronous copies. All of it completes on the slot's "full"
 //    mbarrier. The weight copies of the first slots are issued before the
 //    wait on the previous kernel (they are model state); x after it.
-//  * Warps 0-15 consume: warp w owns columns 32 (w % 8) .. +31 of the tile and
-//    the stage's even (w < 8) or odd (w >= 8) segments, so no partial sums
-//    cross warps inside the CTA. Lane (g = lane / 4, t = lane % 4) owns the
-//    four columns 4g .. 4g+3 (one 16-byte read per word row: eight lanes read
-//    a whole line) and the 8-code block t of every segment. The tile is 248
-//    columns wide so that a word row takes 992 bytes in shared memory: the
-//    four rows that the lanes t = 0..3 of one quarter-warp read then start 6
-//    bank groups apart, and their 16-byte reads do not collide (2-, 3-, 4- and
-//    5-bit segments; 6- and 8-bit ones keep a two-way overlap). Codes are
-//    planted in the mantissa of 1024 (0x6400 | code << p), the zero is taken
-//    off exactly in fp16 and each pair is scaled once (w = fp16_RN((q - z) s),
-//    the definition: the result is x times the rounded fp16 weights), then
-//    fed to mma.sync m16n8k16 (fp16 in, fp32 accumulate) as the A operand of a
-//    swapped product (A = W^T, B = x^T). A stage whose EXL2 segments share one
-//    width runs a loop compiled for that width (one dispatch per stage).
-//  * At the end of a piece each warp writes fp32 partial sums of its 32
-//    columns and K group to the caller's workspace; the warp that arrives
-//    last at its (tile, column group) counter adds the tile's partials in
-//    piece order, writes y and puts the counter back to zero. Deterministic,
-//    and no warp ever waits on another CTA.
+//  * Warps 0-15 consume, in two sets of eight: stage i goes to set i % 2, and
+//    warp w of the set owns columns 32 w .. 32 w + 31 of the tile for every
+//    segment of the stage, so the fixed cost of a stage (wait, descriptor,
+//    release) is paid once per up to 16 segments. Lane (g = lane / 4,
+//    t = lane % 4) owns the four columns 4g .. 4g+3 (one 16-byte read per
+//    word row: eight lanes read a whole line) and the 8-code block t of every
+//    segment. The tile is 248 columns wide so that a word row takes 992 bytes
+//    in shared memory: the four rows that the lanes t = 0..3 of one
+//    quarter-warp read then start 6 bank groups apart, and their 16-byte
+//    reads do not collide. Codes are planted in the mantissa of 1024
+//    (0x6400 | code << p), the zero is taken off exactly in fp16 and each pair
+//    is scaled once (w = fp16_RN((q - z) s), the definition: the result is x
+//    times the rounded fp16 weights), then fed to mma.sync m16n8k16 (fp16 in,
+//    fp32 accumulate) as the A operand of a swapped product (A = W^T,
+//    B = x^T), into four independent accumulators. A stage whose EXL2
+//    segments share one width runs a loop compiled for that width.
+//  * A piece's last stage carries a flush mark; right after it the producer
+//    queues an empty stage with the mark for the other set, so both sets
+//    close every piece. On the mark each warp writes fp32 partial sums of its
+//    32 columns to the caller's workspace; the warp that arrives last at its
+//    (tile, column group) counter adds the tile's partials in piece order,
+//    writes y and puts the counter back to zero. Deterministic, and no warp
+//    ever waits on another CTA.
 //  * An act-order layer's x is gathered into stored-row order by a small
 //    kernel first (into the workspace), once per call rather than per CTA; it
 //    stores each 8-block as x0 x4 x1 x5 x2 x6 x3 x7, so that the consumers
@@ -50,7 +54,9 @@
 //  * EXL2 with two-level scales: instead of the scale box, the stage's rows
 //    of 4-bit scale codes follow as 4-byte asynchronous copies (like GPTQ
 //    zeros) and the tile's fp16 column maxima as one 16-byte copy per lane;
-//    the consumers form each segment's scales as fp16_RN(((c + 1) / 16) m).
+//    the consumers multiply each pair by the exact fraction (c + 1) / 16 and
+//    then by the maximum m, so w = fp16_RN((q - z) ((c + 1) / 16) m) takes
+//    one rounding.
 //  * Programmatic dependent launch: every kernel lets the next launch start
 //    early; the GEMV's first weight copies do not wait for the previous
 //    kernel, its activations and outputs do.
@@ -75,34 +81,42 @@ __device__ unsigned g_gemv_err;
 constexpr int kTN = 248;                 // columns per tile (992-byte rows: see above)
 constexpr int kTP = 256;                 // columns per tile in the partial sums (8 warps x 32)
 constexpr int kColGroups = 8;            // 32 columns each
-constexpr int kConsumerWarps = 2 * kColGroups;  // two K groups: even / odd segments of a stage
+constexpr int kSets = 2;                 // consumer sets: stage i is read by set i % 2
+constexpr int kConsumerWarps = kSets * kColGroups;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kSegsPerStage = 8;         // 256 rows of K
+constexpr int kMaxSegs = 16;             // EXL2 segments per stage
+constexpr int kGptqSegs = 8;             // GPTQ segments per stage (256 rows of K); segments per x box
 constexpr int kRowsPerStage = 32;        // packed word rows per stage (box height)
-constexpr int kScaleRows = 8;            // scale (and GPTQ zero) rows per stage
+constexpr int kScaleRows = 16;           // scale (and GPTQ zero) rows per stage
 constexpr int kCounterBytes = 64 * 1024; // workspace counter region (zero between calls)
 constexpr int kMaxStages = 6;
-constexpr long long kWaitLimit = 1ll << 17;  // try_wait rounds (each may sleep kWaitHintNs) before giving up
-constexpr uint32_t kWaitHintNs = 20000;      // a waiting thread sleeps until the phase completes or this long
+constexpr int kWaitLimit = 1 << 17;      // try_wait rounds (each may sleep kWaitHintNs) before giving up
+constexpr uint32_t kWaitHintNs = 20000;  // a waiting thread sleeps until the phase completes or this long
 
-// slot layout (bytes): word rows | scale rows | GPTQ zero rows | x [M][128]
-constexpr int kRowBytes = kTN * 4;                       // 992
+// slot layout (bytes): word rows | scale rows | GPTQ zero rows | x [2][M][256]
+constexpr int kRowBytes = kTN * 4;                         // 992
+constexpr int kScaleRowBytes = kTN * 2;                    // 496
 constexpr int kSlotW = 0;
 constexpr int kSlotS = kSlotW + kRowsPerStage * kRowBytes;
-constexpr int kSlotZ = ((kSlotS + kScaleRows * kTN * 2 + 127) / 128) * 128;
+constexpr int kSlotZ = ((kSlotS + kScaleRows * kScaleRowBytes + 127) / 128) * 128;
 constexpr int kZeroRowBytes = 128;                         // 31 zero words of a tile, one row per group
 constexpr int kSlotX = kSlotZ + kScaleRows * kZeroRowBytes;
-constexpr int kXRowBytes = kSegsPerStage * 32 * 2;         // 512 B per token
-static_assert(kSlotS % 128 == 0 && kSlotX % 128 == 0, "tensor-map destinations start on 128-byte boundaries");
+constexpr int kXBox = 256;                                 // activations per x box (8 segments)
+constexpr int kXBoxBytes = kXBox * 2;                      // per token
+static_assert(kSlotS % 128 == 0 && kSlotZ % 128 == 0 && kSlotX % 128 == 0,
+              "tensor-map destinations start on 128-byte boundaries");
 static_assert(kTN % 8 == 0 && kTN / 8 <= 32, "a tile's zero words fit one warp");
+static_assert(kMaxSegs <= 2 * kGptqSegs, "a stage's activations fit two x boxes");
 
-__host__ __device__ constexpr int slot_bytes_for(int M) { return ((kSlotX + M * kXRowBytes + 1023) / 1024) * 1024; }
+__host__ __device__ constexpr int slot_bytes_for(int M) {
+  return ((kSlotX + 2 * M * kXBoxBytes + 1023) / 1024) * 1024;
+}
 
 constexpr int kMaxLayers = EXQ_GEMV_MAX_LAYERS;  // layers of one launch (they share x and K)
 
 struct GemvMaps {
   CUtensorMap w[kMaxLayers];  // qweight [n_word_rows, N] uint32, box 248 x 32
-  CUtensorMap s[kMaxLayers];  // scales [groups, N] fp16, box 248 x 8
+  CUtensorMap s[kMaxLayers];  // scales [groups, N] fp16, box 248 x 16
   CUtensorMap x;              // activations [rows, K] fp16 (stored-row order), box 256 x M
 };
 
@@ -134,6 +148,8 @@ struct GemvArgs {
   int stages;
   int slot_bytes;
   int off_bar;              // byte offset of the barriers, descriptors and tables
+  int wait_limit;           // polling rounds of a bounded wait (kWaitLimit unless a test lowers it)
+  int starve;               // test hook: the producer issues nothing, so the consumers' waits run out
 };
 
 // the layer that owns global tile T (constant indices into the parameters)
@@ -153,19 +169,17 @@ __device__ __forceinline__ GemvLayer layer_params(const GemvArgs& a, int L) {
 }
 
 // Stage descriptor, written by the producer before the slot's copies.
-// The consumer K groups take the first h = (count + 1) / 2 segments and the rest.
-//   a: first segment | count << 16 | first-of-piece << 20 | last-of-piece << 21
-//      | end << 22 | uniform width << 23 | H << 24, H = the second half's first word row in the slot
-//      (EXL2) or its scale / zero row (GPTQ)
-//   b: EXL2: widths, 4 bits per segment (0 = skip the segment);
-//      GPTQ: position in its group of the first segment | of the second half's << 16
+//   a: segments n (0..16) | flags
+//   wlo, whi: EXL2 widths, 4 bits per segment (segments 0-7, 8-15; 0 = skip)
 //   c: tile (global over the launch's layers) | layer << 16
-//   d: first scale row of the slot (GPTQ group / EXL2 segment)
+//   gpos: GPTQ: position in its group of the stage's first segment
 struct Desc {
-  uint32_t a, b, c, d;
+  uint32_t a, wlo, whi, c;
+  uint32_t gpos, pad0, pad1, pad2;
 };
-constexpr uint32_t kDescFirst = 1u << 20, kDescLast = 1u << 21, kDescEnd = 1u << 22;
-constexpr uint32_t kDescUniform = 1u << 23;  // EXL2: every segment of the stage has the same width
+constexpr uint32_t kDescLast = 1u << 8;     // after this stage the set flushes its partial sums
+constexpr uint32_t kDescEnd = 1u << 9;      // no more stages for this set
+constexpr uint32_t kDescUniform = 1u << 10; // EXL2: every segment of the stage has the same width
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -200,9 +214,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait by lane 0 of a warp, result broadcast to the warp (all lanes
 // leave in the same round). A timeout is recorded and raises the abort flag;
 // a raised flag makes every other waiter give up too.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int limit) {
   const bool leader = (threadIdx.x & 31) == 0;
-  for (long long i = 0; i < kWaitLimit; ++i) {
+  for (int i = 0; i < limit; ++i) {
     int state = 0;  // 1 = phase complete, 2 = another role gave up
     if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
     state = __shfl_sync(0xffffffffu, state, 0);
@@ -255,23 +269,27 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int c) {
   return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
 
-
 // ---------------------------------------------------------------- one segment
 // Lane (g, t) holds, for its four columns c = 0..3, the exact fp16 pairs
 // P[c][i] = (v_i - z, v_{i+4} - z) of the codes v_0..v_7 of block t. The MMA
 // rows are the columns: tile 0 = columns 0 (row g) and 1 (row g + 8), tile 1
-// = columns 2 and 3. Slab 0 takes pairs 0 and 1, slab 1 pairs 2 and 3; the
-// activations xb[mt] hold the matching pairs of token g (+ 8 mt).
+// = columns 2 and 3. Slab 0 takes pairs 0 and 1, slab 1 pairs 2 and 3; each
+// (tile, slab) has its own accumulator, so the four MMAs of a segment do not
+// wait on one another. The activations xb[mt] hold the matching pairs of
+// token g (+ 8 mt).
 
 template <int MT>
-__device__ __forceinline__ void seg_mma(float (&D)[MT][2][4], const uint32_t (&P)[4][4], const uint32_t (&xb)[MT][4]) {
+using Acc = float[MT][2][2][4];
+
+template <int MT>
+__device__ __forceinline__ void seg_mma(Acc<MT>& D, const uint32_t (&P)[4][4], const uint32_t (&xb)[MT][4]) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int c = 2 * h;
-      mma16816(D[mt][h], P[c][0], P[c + 1][0], P[c][1], P[c + 1][1], xb[mt][0], xb[mt][1]);
-      mma16816(D[mt][h], P[c][2], P[c + 1][2], P[c][3], P[c + 1][3], xb[mt][2], xb[mt][3]);
+      mma16816(D[mt][h][0], P[c][0], P[c + 1][0], P[c][1], P[c + 1][1], xb[mt][0], xb[mt][1]);
+      mma16816(D[mt][h][1], P[c][2], P[c + 1][2], P[c][3], P[c + 1][3], xb[mt][2], xb[mt][3]);
     }
   }
 }
@@ -300,66 +318,54 @@ __device__ __forceinline__ void exl2_unpack(const uint8_t* row, uint32_t off, ui
   }
 }
 
-// the lane's four scales of one scale row: s2[c] is the word holding column
-// c's scale, in its low half for even c and its high half for odd c
+// The lane's four column scales, each in both halves of a word, from one
+// 8-byte read of a scale row.
 __device__ __forceinline__ void scales4(const uint8_t* p, uint32_t (&s2)[4]) {
   const uint2 v = lds64(p);
-  s2[0] = s2[1] = v.x;
-  s2[2] = s2[3] = v.y;
+  s2[0] = prmt(v.x, v.x, 0x1010);
+  s2[1] = prmt(v.x, v.x, 0x3232);
+  s2[2] = prmt(v.y, v.y, 0x1010);
+  s2[3] = prmt(v.y, v.y, 0x3232);
 }
 
-// the same from two-level scales: `codes` = the lane's four 4-bit codes in
-// its low 16 bits, mv = the four columns' fp16 maxima
-__device__ __forceinline__ void qscales4(uint32_t codes, const uint2& mv, uint32_t (&s2)[4]) {
+// two-level scales: the exact fractions (c + 1) / 16 of the lane's four
+// columns, each in both halves of a word; `codes` = their 4-bit codes in the
+// low 16 bits
+__device__ __forceinline__ void qfracs4(uint32_t codes, uint32_t (&s2)[4]) {
   const uint32_t lo = codes & 0xFFFFu, hi = lo >> 8;
-  const uint32_t a = two_level_scale2(lo | (lo << 12), mv.x);  // columns 0, 1
-  const uint32_t b = two_level_scale2(hi | (hi << 12), mv.y);  // columns 2, 3
-  s2[0] = s2[1] = a;
-  s2[2] = s2[3] = b;
+  const uint32_t a = two_level_frac2(lo | (lo << 12));  // columns 0, 1
+  const uint32_t b = two_level_frac2(hi | (hi << 12));  // columns 2, 3
+  s2[0] = prmt(a, a, 0x1010);
+  s2[1] = prmt(a, a, 0x3232);
+  s2[2] = prmt(b, b, 0x1010);
+  s2[3] = prmt(b, b, 0x3232);
 }
 
-__device__ __forceinline__ __half2 as_h2(uint32_t v) {
-  __half2 h;
-  memcpy(&h, &v, 4);
-  return h;
-}
-__device__ __forceinline__ uint32_t as_u32(__half2 h) {
-  uint32_t v;
-  memcpy(&v, &h, 4);
-  return v;
-}
-
-// w = fp16_RN((q - z) s) for the lane's four columns: each pair times the
-// low or the high half of its scale word, broadcast (one fp16 multiply,
-// round to nearest even)
-__device__ __forceinline__ void scale_pairs(uint32_t (&P)[4][4], const uint32_t (&s2)[4]) {
+// w = fp16_RN((q - z) s) for the lane's four columns: one fp16 multiply per
+// pair, round to nearest even. Two-level scales: s2 = the exact fractions,
+// m2 = the column maxima; (q - z) (c + 1) / 16 is exact and the multiply by
+// the maximum is the one rounding.
+template <int FMT>
+__device__ __forceinline__ void scale_pairs(uint32_t (&P)[4][4], const uint32_t (&s2)[4], const uint32_t (&m2)[4]) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const __half2 s = (c & 1) ? __high2half2(as_h2(s2[c])) : __low2half2(as_h2(s2[c]));
+  for (int c = 0; c < 4; ++c)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) P[c][i] = as_u32(__hmul2_rn(as_h2(P[c][i]), s));
-  }
-}
-
-// one EXL2 segment of width B, whole: unpack, scale, multiply (each width
-// keeps its own registers from the unpack to the MMA)
-template <int B, int MT>
-__device__ __forceinline__ void exl2_seg(const uint8_t* row, uint32_t off, const uint32_t (&xb)[MT][4],
-                                         const uint32_t (&s2)[4], float (&acc)[MT][2][4]) {
-  uint32_t P[4][4];
-  exl2_unpack<B>(row, off, P);
-  scale_pairs(P, s2);
-  seg_mma<MT>(acc, P, xb);
+    for (int i = 0; i < 4; ++i) {
+      P[c][i] = hmul2(P[c][i], s2[c]);
+      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) P[c][i] = hmul2(P[c][i], m2[c]);
+    }
 }
 
 template <int MT>
-__device__ __forceinline__ void zero4(float (&a)[MT][2][4]) {
+__device__ __forceinline__ void zero_acc(Acc<MT>& a) {
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[mt][h][i] = 0.f;
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[mt][h][k][i] = 0.f;
 }
 
 // the pairs (x0,x4),(x1,x5),(x2,x6),(x3,x7) of 8 consecutive activations
@@ -367,19 +373,37 @@ __device__ __forceinline__ void zero4(float (&a)[MT][2][4]) {
 // x0 x4 x1 x5 x2 x6 x3 x7, so the words are the pairs)
 template <bool XP>
 __device__ __forceinline__ void x_pairs(const uint8_t* p, uint32_t (&xb)[4]) {
+  const uint4 v = lds128(p);
   if constexpr (XP) {
-    const uint4 v = lds128(p);
     xb[0] = v.x;
     xb[1] = v.y;
     xb[2] = v.z;
     xb[3] = v.w;
-    return;
+  } else {
+    xb[0] = prmt(v.x, v.z, 0x5410);
+    xb[1] = prmt(v.x, v.z, 0x7632);
+    xb[2] = prmt(v.y, v.w, 0x5410);
+    xb[3] = prmt(v.y, v.w, 0x7632);
   }
-  const uint4 v = lds128(p);
-  xb[0] = prmt(v.x, v.z, 0x5410);
-  xb[1] = prmt(v.x, v.z, 0x7632);
-  xb[2] = prmt(v.y, v.w, 0x5410);
-  xb[3] = prmt(v.y, v.w, 0x7632);
+}
+
+// activations of token tiles 0 (and 1) for one segment; dx = byte distance
+// from the lane's token of tile 0 to its token of tile 1
+template <int MT, bool XP>
+__device__ __forceinline__ void load_x(const uint8_t* xp, int dx, uint32_t (&xb)[MT][4]) {
+  x_pairs<XP>(xp, xb[0]);
+  if constexpr (MT == 2) x_pairs<XP>(xp + dx, xb[1]);
+}
+
+// Lane t's 8-code block of a width-B segment starts at stream bit 8 B t:
+// byte offset of its first word row (relative to the segment) and bit offset.
+template <int B>
+__device__ __forceinline__ int blk_row_bytes(int t) {
+  return ((8 * B * t) >> 5) * kRowBytes;
+}
+template <int B>
+__device__ __forceinline__ uint32_t blk_bit(int t) {
+  return static_cast<uint32_t>((8 * B * t) & 31);
 }
 
 // ---------------------------------------------------------------- work split
@@ -433,6 +457,61 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint16_t* __restric
 
 __device__ __forceinline__ bool valid_width(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
 
+// ---------------------------------------------------------------- consumers of one stage
+// Pointers of a consumer lane into one slot: wp = its columns of the first
+// word row, sp = its four scales of the first scale row, xp = its activations
+// of the first segment, cp = its scale codes (two-level) of the first segment.
+
+// EXL2, every segment of width B: n segments from those pointers
+template <int FMT, int B, int MT, bool XP>
+__device__ __forceinline__ void run_uniform(const uint8_t* wp, const uint8_t* sp, const uint8_t* xp, int dx,
+                                            int t, int n, const uint32_t (&m2)[4], const uint8_t* cp, int csh,
+                                            Acc<MT>& acc) {
+  const uint8_t* wrow = wp + blk_row_bytes<B>(t);
+  const uint32_t off = blk_bit<B>(t);
+#pragma unroll 2
+  for (int j = 0; j < n; ++j) {
+    uint32_t xb[MT][4], s2[4], P[4][4];
+    load_x<MT, XP>(xp + 64 * j, dx, xb);
+    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+      qfracs4(lds32(cp + j * kZeroRowBytes) >> csh, s2);
+    else
+      scales4(sp + j * kScaleRowBytes, s2);
+    exl2_unpack<B>(wrow + j * (B * kRowBytes), off, P);
+    scale_pairs<FMT>(P, s2, m2);
+    seg_mma<MT>(acc, P, xb);
+  }
+}
+
+// EXL2, widths from the descriptor (4 bits per segment): n segments of one x
+// box; returns the word row after them
+template <int FMT, int MT, bool XP>
+__device__ __forceinline__ const uint8_t* run_mixed(const uint8_t* row, const uint8_t* sp, const uint8_t* xp, int dx,
+                                                    int t, int n, uint32_t widths, const uint32_t (&m2)[4],
+                                                    const uint8_t* cp, int csh, Acc<MT>& acc) {
+  for (int j = 0; j < n; ++j, widths >>= 4) {
+    const int b = static_cast<int>(widths & 15u);
+    if (b == 0) continue;  // a segment the producer rejected (reported); it takes no rows
+    uint32_t xb[MT][4], s2[4], P[4][4];
+    load_x<MT, XP>(xp + 64 * j, dx, xb);
+    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+      qfracs4(lds32(cp + j * kZeroRowBytes) >> csh, s2);
+    else
+      scales4(sp + j * kScaleRowBytes, s2);
+    switch (b) {
+      case 2: exl2_unpack<2>(row + blk_row_bytes<2>(t), blk_bit<2>(t), P); row += 2 * kRowBytes; break;
+      case 3: exl2_unpack<3>(row + blk_row_bytes<3>(t), blk_bit<3>(t), P); row += 3 * kRowBytes; break;
+      case 4: exl2_unpack<4>(row + blk_row_bytes<4>(t), blk_bit<4>(t), P); row += 4 * kRowBytes; break;
+      case 5: exl2_unpack<5>(row + blk_row_bytes<5>(t), blk_bit<5>(t), P); row += 5 * kRowBytes; break;
+      case 6: exl2_unpack<6>(row + blk_row_bytes<6>(t), blk_bit<6>(t), P); row += 6 * kRowBytes; break;
+      default: exl2_unpack<8>(row + blk_row_bytes<8>(t), blk_bit<8>(t), P); row += 8 * kRowBytes; break;
+    }
+    scale_pairs<FMT>(P, s2, m2);
+    seg_mma<MT>(acc, P, xb);
+  }
+  return row;
+}
+
 // ---------------------------------------------------------------- the kernel
 // MT: 8-token blocks (1 for M <= 8, 2 for M <= 16).
 
@@ -454,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kConsumerWarps);  // every consumer warp reads every stage
+      mbar_init(smem_u32(&empty[i]), kColGroups);  // the eight warps of the stage's set read it
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -467,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    if (a.starve) return;  // test hook: nothing is issued, nothing is in flight
     // the layers this CTA's share touches
     const int la = layer_of(a, u0 / a.S), lb = layer_of(a, (u1 - 1) / a.S);
     if (lane == 0) {
@@ -488,9 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("cp.async.wait_all;" ::: "memory");
       __syncwarp();
     }
-    const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXRowBytes;
+    const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXBoxBytes;  // one x box
     // two-level scales arrive by cp.async, not in the transaction count
-    const uint32_t tx = kRowsPerStage * kTN * 4 + (FMT == EXQ_FMT_EXL2_QSCALE ? 0 : kScaleRows * kTN * 2) + x_bytes;
+    const uint32_t tx_w = kRowsPerStage * kTN * 4 + (FMT == EXQ_FMT_EXL2_QSCALE ? 0 : kScaleRows * kTN * 2);
     int slot = 0, ephase = 0, issued = 0, npend = 0;
     // the piece's layer: its index, tensor maps, first row of x, GPTQ zeros
     const CUtensorMap* mw = &maps.w[0];
@@ -499,33 +579,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t* qz = nullptr;                // GPTQ zeros or two-level scale codes
     const uint16_t* qmax = nullptr;
     bool waited = false, ok = true;
+    auto x_copies = [&](int sl, int seg, int nx, int xr) {
+      uint8_t* st = smem + sl * a.slot_bytes;
+      for (int b = 0; b < nx; ++b)
+        tma_load_2d(smem_u32(st + kSlotX + b * a.M * kXBoxBytes), &maps.x, seg * 32 + b * kXBox, xr,
+                    smem_u32(&full[sl]));
+    };
     auto release_x = [&]() {  // the activations may be read once the previous kernel is done
       asm volatile("griddepcontrol.wait;" ::: "memory");
       if (lane == 0)
-        for (int i = 0; i < npend; ++i) {
-          const int sl = pend[i] & 0xFF, seg = (pend[i] >> 8) & 0xFFFF, xr = static_cast<int>(pend[i] >> 24);
-          tma_load_2d(smem_u32(smem + sl * a.slot_bytes + kSlotX), &maps.x, seg * 32, xr, smem_u32(&full[sl]));
-        }
+        for (int i = 0; i < npend; ++i)
+          x_copies(pend[i] & 0x7F, (pend[i] >> 8) & 0xFFFF, (pend[i] & 0x80) ? 2 : 1,
+                   static_cast<int>(static_cast<unsigned>(pend[i]) >> 24));
       npend = 0;
       waited = true;
     };
+    auto next_slot = [&]() {
+      ++issued;
+      if (++slot == a.stages) {
+        slot = 0;
+        ephase ^= 1;
+      }
+    };
     // one stage into the next slot; false once a wait gave up
     // tile: global (for the consumers), lt: in the layer (for the copies)
-    auto issue = [&](uint32_t da, uint32_t widths, int tile, int lt, int row0, int srow, bool bad) -> bool {
+    auto issue = [&](uint32_t da, uint32_t wlo, uint32_t whi, uint32_t gpos, int tile, int lt, int seg, int n,
+                     int row0, int srow, int zrows, bool bad) -> bool {
       if (!waited && issued >= a.stages) release_x();  // the ring is about to wrap
-      if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag)) return false;
+      if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag, a.wait_limit)) return false;
       uint8_t* st = smem + slot * a.slot_bytes;
       const uint32_t fb = smem_u32(&full[slot]);
       if (lane == 0)
-        desc[slot] = Desc{da, widths, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16),
-                          static_cast<uint32_t>(srow)};
+        desc[slot] = Desc{da, wlo, whi, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16), gpos,
+                          0u, 0u, 0u};
+      const int nx = n > kGptqSegs ? 2 : 1;
       if constexpr (FMT != EXQ_FMT_EXL2) {
         if (!bad) {
           // GPTQ zero rows or two-level scale-code rows: [rows, N / 8] words
           const int cw = lt * (kTN / 8) + lane;
-#pragma unroll
-          for (int r = 0; r < kScaleRows; ++r)
-            if (srow + r < a.G && cw < nz && lane < kTN / 8)
+          for (int r = 0; r < zrows; ++r)
+            if (cw < nz && lane < kTN / 8)
               cp_async4(smem_u32(st + kSlotZ + r * kZeroRowBytes + lane * 4),
                         qz + static_cast<size_t>(srow + r) * nz + cw);
           // two-level: the tile's column maxima, 8 columns (16 bytes) per lane
@@ -539,18 +632,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bad) {
           mbar_arrive(fb);
         } else {
-          mbar_expect_tx(fb, tx);
+          mbar_expect_tx(fb, tx_w + nx * x_bytes);
           tma_load_2d(smem_u32(st + kSlotW), mw, lt * kTN, row0, fb);
           if constexpr (FMT != EXQ_FMT_EXL2_QSCALE) tma_load_2d(smem_u32(st + kSlotS), ms, lt * kTN, srow, fb);
-          if (waited) tma_load_2d(smem_u32(st + kSlotX), &maps.x, static_cast<int>(da & 0xFFFFu) * 32, xrow, fb);
+          if (waited) x_copies(slot, seg, nx, xrow);
         }
       }
-      if (!bad && !waited) pend[npend++] = slot | (static_cast<int>(da & 0xFFFFu) << 8) | (xrow << 24);
-      ++issued;
-      if (++slot == a.stages) {
-        slot = 0;
-        ephase ^= 1;
+      if (!bad && !waited) pend[npend++] = slot | (nx == 2 ? 0x80 : 0) | (seg << 8) | (xrow << 24);
+      next_slot();
+      return true;
+    };
+    // a stage without data: only its descriptor (a flush mark, with the
+    // piece's tile and layer, or an end mark)
+    auto mark = [&](uint32_t da, uint32_t dc) -> bool {
+      if (!waited && issued >= a.stages) release_x();
+      if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag, a.wait_limit)) return false;
+      if (lane == 0) {
+        desc[slot] = Desc{da, 0u, 0u, dc, 0u, 0u, 0u, 0u};
+        mbar_arrive(smem_u32(&full[slot]));
       }
+      next_slot();
       return true;
     };
 
@@ -569,80 +670,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sa = u - tile * a.S;
       const int sb = min(a.S, sa + (u1 - u));
       u += sb - sa;
-      bool first = true;
       for (int seg = sa; seg < sb && ok;) {
-        int n, row0, srow;
-        uint32_t widths = 0;
-        int ps_h = 0;  // EXL2: this lane's inclusive prefix sum of the stage's widths
-        bool bad = false;
+        int n, row0, srow, zrows = 0;
+        uint32_t wlo = 0, whi = 0, gpos = 0;
+        bool bad = false, uniform = false;
         if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          n = min(sb, (seg / kSegsPerStage + 1) * kSegsPerStage) - seg;
+          n = min(sb, (seg / kGptqSegs + 1) * kGptqSegs) - seg;
           row0 = 4 * seg;
           srow = seg / a.gs_seg;
+          gpos = static_cast<uint32_t>(seg - srow * a.gs_seg);
+          zrows = (seg + n - 1) / a.gs_seg - srow + 1;
         } else {
           // greedy, one candidate segment per lane: the longest run of valid
-          // segments from seg (at most eight) whose widths add up to at most 32
+          // segments from seg (at most sixteen) whose widths add up to at most 32
           const int sk = seg + lane;
-          const bool cand = lane < kSegsPerStage && sk < sb;
+          const bool cand = lane < kMaxSegs && sk < sb;
           const uint32_t* ltbl = tbl + layer * (a.S + 1);
           const uint32_t e0 = cand ? ltbl[sk] : 0u, e1 = cand ? ltbl[sk + 1] : 0u;
           const int b = static_cast<int>(e1) - static_cast<int>(e0);
           const bool good = cand && valid_width(b) && e1 <= static_cast<uint32_t>(ly.n_word_rows);
-          int ps = good ? b : 0;  // inclusive prefix sum of the widths over lanes 0..7
+          int ps = good ? b : 0;  // inclusive prefix sum of the widths over lanes 0..15
 #pragma unroll
-          for (int d = 1; d < 8; d <<= 1) {
+          for (int d = 1; d < kMaxSegs; d <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, ps, d);
             if (lane >= d) ps += v;
           }
           const unsigned stop = __ballot_sync(0xffffffffu, !(good && ps <= kRowsPerStage));
-          n = __ffs(stop) - 1;  // leading lanes that fit (stop always has a bit at or below lane 4)
-          widths = __reduce_or_sync(0xffffffffu, lane < n ? static_cast<uint32_t>(b) << (4 * lane) : 0u);
-          ps_h = ps;
+          n = __ffs(stop) - 1;  // leading lanes that fit (stop always has a bit at or below lane 16)
+          wlo = __reduce_or_sync(0xffffffffu, lane < n && lane < 8 ? static_cast<uint32_t>(b) << (4 * lane) : 0u);
+          whi = __reduce_or_sync(0xffffffffu,
+                                 lane < n && lane >= 8 ? static_cast<uint32_t>(b) << (4 * (lane - 8)) : 0u);
           row0 = static_cast<int>(__shfl_sync(0xffffffffu, e0, 0));
           srow = seg;
+          zrows = n;
           if (n == 0) {  // the segment at seg itself is malformed: skip it alone, reported
             bad = true;
             n = 1;
             if (lane == 0) atomicOr(&g_gemv_err, kDevErrBadSegment);
+          } else {
+            const uint32_t rep = (wlo & 15u) * 0x11111111u;
+            const uint32_t mlo = n >= 8 ? ~0u : (1u << (4 * n)) - 1u;
+            const uint32_t mhi = n <= 8 ? 0u : n >= 16 ? ~0u : (1u << (4 * (n - 8))) - 1u;
+            uniform = ((wlo ^ rep) & mlo) == 0 && ((whi ^ rep) & mhi) == 0;
           }
         }
         const bool last = seg + n == sb;
-        const int h = (n + 1) >> 1;  // segments of the first consumer K group
-        uint32_t half, db;
-        if constexpr (FMT == EXQ_FMT_GPTQ4) {
-          const int gh = (seg + h) / a.gs_seg;
-          half = static_cast<uint32_t>(gh - srow);
-          db = static_cast<uint32_t>(seg - srow * a.gs_seg) | (static_cast<uint32_t>(seg + h - gh * a.gs_seg) << 16);
-        } else {
-          half = static_cast<uint32_t>(__shfl_sync(0xffffffffu, ps_h, h - 1));
-          db = widths;
-        }
-        bool uniform = false;
-        if constexpr (FMT != EXQ_FMT_GPTQ4) {
-          const uint32_t b0 = widths & 15u;
-          const uint32_t used = n >= 8 ? ~0u : (1u << (4 * n)) - 1u;
-          uniform = !bad && ((widths ^ (b0 * 0x11111111u)) & used) == 0;
-        }
-        const uint32_t da = static_cast<uint32_t>(seg) | (static_cast<uint32_t>(n) << 16) | (first ? kDescFirst : 0u) |
-                            (uniform ? kDescUniform : 0u) |
-                            (last ? kDescLast : 0u) | (half << 24);
-        ok = issue(da, db, tile, lt, row0, srow, bad);
+        const uint32_t da = static_cast<uint32_t>(n) | (last ? kDescLast : 0u) | (uniform ? kDescUniform : 0u);
+        ok = issue(da, wlo, whi, gpos, tile, lt, seg, n, row0, srow, zrows, bad);
         seg += n;
-        first = false;
       }
+      // the other set closes the piece too
+      if (ok) ok = mark(kDescLast, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16));
     }
     if (!waited) release_x();
-    const bool ended = ok && warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag);
-    if (ended && lane == 0) {
-      desc[slot] = Desc{kDescEnd, 0u, 0u, 0u};
-      mbar_arrive(smem_u32(&full[slot]));
-    }
+    // one end mark per set
+    const bool ended = ok && mark(kDescEnd, 0u) && mark(kDescEnd, 0u);
     // after a give-up no consumer will wait for the copies still in flight:
     // they land before the CTA may exit (otherwise the consumers saw them all)
     if (!ended && lane == 0)
       for (int i = max(0, issued - a.stages); i < issued; ++i) {
         const uint32_t bar = smem_u32(&full[i % a.stages]);
-        for (long long r = 0; r < kWaitLimit; ++r)
+        for (int r = 0; r < a.wait_limit; ++r)
           if (mbar_try_wait(bar, (i / a.stages) & 1)) break;
       }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -652,124 +740,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   // -------------------------------------------------------------- consumers
   asm volatile("griddepcontrol.wait;" ::: "memory");  // y and the workspace are shared with earlier kernels
   const int g = lane >> 2, t = lane & 3;
-  const int w = warp & (kColGroups - 1);  // column group: columns 32w .. 32w+31 of the tile
-  const int kg = warp / kColGroups;       // K group: the stage's segments j with j % 2 == kg
-  const int tok[2] = {min(g, a.M - 1), min(g + 8, a.M - 1)};
-  float acc[MT][2][4];
-  zero4<MT>(acc);
-  uint32_t zlo[4] = {0u, 0u, 0u, 0u}, zhi[4] = {0u, 0u, 0u, 0u}, s2[4] = {0u, 0u, 0u, 0u};
-  int slot = 0, fphase = 0;
+  const int set = warp / kColGroups;
+  const int w = warp % kColGroups;         // column group: columns 32w .. 32w+31 of the tile
+  const int tok0 = min(g, a.M - 1), tok1 = min(g + 8, a.M - 1);
+  const int lw = kSlotW + 128 * w + 16 * g;                   // the lane's columns in a word row
+  const int ls = kSlotS + 64 * w + 8 * g;                     // its four scales in a scale row
+  const int lx = kSlotX + tok0 * kXBoxBytes + 16 * t;         // its block of x, token tile 0
+  const int dx = (tok1 - tok0) * kXBoxBytes;                  // to token tile 1
+  const int xbox = a.M * kXBoxBytes;                          // to the second x box
+  const int lc = kSlotZ + (4 * w + (g >> 1)) * 4;             // its zero word (GPTQ) / scale codes (two-level)
+  const int csh = 16 * (g & 1);                               // its nibbles in that word
+  Acc<MT> acc;
+  zero_acc<MT>(acc);
+  int slot = set, fphase = 0;  // this set's first stage (stages >= 2)
   for (;;) {
-    if (!warp_wait(smem_u32(&full[slot]), fphase, abort_flag)) break;
+    if (!warp_wait(smem_u32(&full[slot]), fphase, abort_flag, a.wait_limit)) break;
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
     const uint8_t* sl = smem + slot * a.slot_bytes;
-    const int n = static_cast<int>((d.a >> 16) & 15u);
-    if (d.a & kDescFirst) zero4<MT>(acc);
-    const uint8_t* wrow = sl + kSlotW + 128 * w + 16 * g;
-    const uint8_t* xrow0 = sl + kSlotX + tok[0] * kXRowBytes + 16 * t;
-    const uint8_t* xrow1 = sl + kSlotX + tok[1] * kXRowBytes + 16 * t;
-    const int col_off = 64 * w + 8 * g;  // byte offset of the lane's 4 scales in a scale row
-    const int h = (n + 1) >> 1;
-    const int j0 = kg ? h : 0, j1 = kg ? n : h;  // this K group's segments of the stage
+    const int n = static_cast<int>(d.a & 31u);
     if constexpr (FMT != EXQ_FMT_GPTQ4) {
-      const uint32_t widths = d.b;
       // two-level: the lane's four column maxima (the same for every segment of the tile)
-      uint2 mv = make_uint2(0u, 0u);
-      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) mv = lds64(sl + kSlotS + col_off);
-      int o = kg ? static_cast<int>(d.a >> 24) : 0;  // word row of segment j0 in the slot
-      // a stage of one width: the width is known for the whole run
-      auto run = [&](auto width) {
-        constexpr int B = decltype(width)::value;
-#pragma unroll 2
-        for (int j = j0; j < j1; ++j, o += B) {
-          uint32_t xb[MT][4];
-          x_pairs<XP>(xrow0 + 64 * j, xb[0]);
-          if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
-          if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
-            qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
-          else
-            scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
-          const int bit = 8 * B * t;
-          exl2_seg<B, MT>(wrow + (o + (bit >> 5)) * kRowBytes, static_cast<uint32_t>(bit & 31), xb, s2, acc);
-        }
-      };
+      uint32_t m2[4] = {0u, 0u, 0u, 0u};
+      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) scales4(sl + ls, m2);
+      const int n0 = min(n, kGptqSegs);
       if (d.a & kDescUniform) {
-        switch (widths & 15u) {
-          case 2: run(std::integral_constant<int, 2>{}); break;
-          case 3: run(std::integral_constant<int, 3>{}); break;
-          case 4: run(std::integral_constant<int, 4>{}); break;
-          case 5: run(std::integral_constant<int, 5>{}); break;
-          case 6: run(std::integral_constant<int, 6>{}); break;
-          default: run(std::integral_constant<int, 8>{}); break;
+        auto uni = [&](auto width) {
+          constexpr int B = decltype(width)::value;
+          run_uniform<FMT, B, MT, XP>(sl + lw, sl + ls, sl + lx, dx, t, n0, m2, sl + lc, csh, acc);
+          if (n > kGptqSegs)
+            run_uniform<FMT, B, MT, XP>(sl + lw + kGptqSegs * B * kRowBytes, sl + ls + kGptqSegs * kScaleRowBytes,
+                                        sl + lx + xbox, dx, t, n - kGptqSegs, m2,
+                                        sl + lc + kGptqSegs * kZeroRowBytes, csh, acc);
+        };
+        switch (d.wlo & 15u) {
+          case 2: uni(std::integral_constant<int, 2>{}); break;
+          case 3: uni(std::integral_constant<int, 3>{}); break;
+          case 4: uni(std::integral_constant<int, 4>{}); break;
+          case 5: uni(std::integral_constant<int, 5>{}); break;
+          case 6: uni(std::integral_constant<int, 6>{}); break;
+          default: uni(std::integral_constant<int, 8>{}); break;
         }
-      } else
-      for (int j = j0; j < j1; ++j) {
-        const int b = static_cast<int>((widths >> (4 * j)) & 15u);
-        if (b != 0) {  // 0: a segment the producer rejected (reported)
-          uint32_t xb[MT][4];
-          x_pairs<XP>(xrow0 + 64 * j, xb[0]);
-          if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
-          if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
-            qscales4(lds32(sl + kSlotZ + j * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1)), mv, s2);
-          else
-            scales4(sl + kSlotS + j * (kTN * 2) + col_off, s2);
-          const int bit = 8 * t * b;
-          const uint8_t* row = wrow + (o + (bit >> 5)) * kRowBytes;
-          const uint32_t off = static_cast<uint32_t>(bit & 31);
-          switch (b) {
-            case 2: exl2_seg<2, MT>(row, off, xb, s2, acc); break;
-            case 3: exl2_seg<3, MT>(row, off, xb, s2, acc); break;
-            case 4: exl2_seg<4, MT>(row, off, xb, s2, acc); break;
-            case 5: exl2_seg<5, MT>(row, off, xb, s2, acc); break;
-            case 6: exl2_seg<6, MT>(row, off, xb, s2, acc); break;
-            default: exl2_seg<8, MT>(row, off, xb, s2, acc); break;
-          }
-        }
-        o += b;
+      } else {
+        const uint8_t* row =
+            run_mixed<FMT, MT, XP>(sl + lw, sl + ls, sl + lx, dx, t, n0, d.wlo, m2, sl + lc, csh, acc);
+        if (n > kGptqSegs)
+          run_mixed<FMT, MT, XP>(row, sl + ls + kGptqSegs * kScaleRowBytes, sl + lx + xbox, dx, t, n - kGptqSegs,
+                                 d.whi, m2, sl + lc + kGptqSegs * kZeroRowBytes, csh, acc);
       }
     } else {
-      int rem = static_cast<int>(kg ? (d.b >> 16) : (d.b & 0xFFFFu));  // position of segment j0 in its group
-      int r = kg ? static_cast<int>(d.a >> 24) : 0;                       // its scale / zero row in the slot
-      int loaded = -1;  // the row whose zeros and scales are in registers
-      for (int j = j0; j < j1; ++j) {
-        if (r != loaded) {  // this warp's first segment of the slot, or a new group
-          loaded = r;
-          const uint32_t zw = lds32(sl + kSlotZ + r * kZeroRowBytes + (4 * w + (g >> 1)) * 4) >> (16 * (g & 1));
+      int rem = static_cast<int>(d.gpos);  // position of the stage's first segment in its group
+      const uint8_t* zr = sl + lc;         // zero word of the current group
+      const uint8_t* sr = sl + ls;         // scales of the current group
+      const uint8_t* wr = sl + lw + t * kRowBytes;
+      const uint8_t* xr = sl + lx;
+      uint32_t zlo[4], zhi[4], s2[4];
+      for (int j = 0; j < n; ++j) {
+        if (j == 0 || rem == 0) {  // this stage's first segment, or a new group
+          const uint32_t zw = lds32(zr) >> csh;
 #pragma unroll
           for (int c = 0; c < 4; ++c) gptq_zero_consts((zw >> (4 * c)) & 0xFu, zlo[c], zhi[c]);
-          scales4(sl + kSlotS + r * (kTN * 2) + col_off, s2);
+          scales4(sr, s2);
         }
         uint32_t xb[MT][4];
-        x_pairs<XP>(xrow0 + 64 * j, xb[0]);
-        if constexpr (MT == 2) x_pairs<XP>(xrow1 + 64 * j, xb[MT - 1]);
-        const uint4 wq = lds128(wrow + (4 * j + t) * kRowBytes);
+        load_x<MT, XP>(xr, dx, xb);
+        const uint4 wq = lds128(wr);
         uint32_t P[4][4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) unpack8_gptq(comp(wq, c), zlo[c], zhi[c], P[c]);
-        scale_pairs(P, s2);
+        scale_pairs<FMT>(P, s2, s2);
         seg_mma<MT>(acc, P, xb);
+        wr += 4 * kRowBytes;
+        xr += 64;
         if (++rem == a.gs_seg) {
           rem = 0;
-          ++r;
+          zr += kZeroRowBytes;
+          sr += kScaleRowBytes;
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-    if (++slot == a.stages) {
-      slot = 0;
+    slot += kSets;
+    if (slot >= a.stages) {
+      slot -= a.stages;
       fphase ^= 1;
     }
 
     if (d.a & kDescLast) {
-      // ---- this warp's share of the piece: 32 columns, one K group. Every
-      // (piece, K group) leaves fp32 partial sums; the last of the tile's
-      // 2P arrivals at the column group's counter adds them in order.
+      // ---- this warp's share of the piece: 32 columns, one set. Every
+      // (piece, set) leaves fp32 partial sums; the last of the tile's 2P
+      // arrivals at the column group's counter adds them in order.
       const int tile = static_cast<int>(d.c & 0xFFFFu);
       const int first = share_owner(tile * a.S, a.total, G);
-      const int P2 = 2 * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
-      const int pslot = 2 * (static_cast<int>(blockIdx.x) - first) + kg;
+      const int P2 = kSets * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
+      const int pslot = kSets * (static_cast<int>(blockIdx.x) - first) + set;
       float* part = a.partials + (static_cast<size_t>(tile) * a.max_pieces + pslot) * a.M * kTP;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -778,8 +843,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = 8 * mt + 2 * t + hh;
           if (m < a.M)
             *reinterpret_cast<float4*>(part + m * kTP + 32 * w + 4 * g) =
-                make_float4(acc[mt][0][hh], acc[mt][0][2 + hh], acc[mt][1][hh], acc[mt][1][2 + hh]);
+                make_float4(acc[mt][0][0][hh] + acc[mt][0][1][hh], acc[mt][0][0][2 + hh] + acc[mt][0][1][2 + hh],
+                            acc[mt][1][0][hh] + acc[mt][1][1][hh], acc[mt][1][0][2 + hh] + acc[mt][1][1][2 + hh]);
         }
+      zero_acc<MT>(acc);
       // the warp's stores, then one acquire-release increment by lane 0: it
       // publishes them and, for the last arriver, makes every other piece's
       // stores visible to the reads below
@@ -797,8 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (last) {
         const GemvLayer* lp = &a.L[0] + (d.c >> 16);
         const float* base = a.partials + static_cast<size_t>(tile) * a.max_pieces * a.M * kTP + 32 * w + lane;
-        const int n = (tile - lp->tile0) * kTN + 32 * w + lane;
-        const bool n_ok = 32 * w + lane < kTN && n < lp->N;
+        const int ncol = (tile - lp->tile0) * kTN + 32 * w + lane;
+        const bool n_ok = 32 * w + lane < kTN && ncol < lp->N;
         const size_t stride = static_cast<size_t>(a.M) * kTP;
         for (int m = 0; m < a.M; ++m) {
           // pieces added in piece order, 32 loads in flight at a time
@@ -811,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v += q[i];
           }
-          if (n_ok) lp->y[static_cast<size_t>(m) * lp->N + n] = __half_as_ushort(__float2half_rn(v));
+          if (n_ok) lp->y[static_cast<size_t>(m) * lp->N + ncol] = __half_as_ushort(__float2half_rn(v));
         }
       }
     }
@@ -847,7 +914,7 @@ int variant_index(int fmt, int M, bool xp) { return 4 * (fmt - 1) + 2 * (xp ? 1 
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr int kSmemPerCta = 210 * 1024;  // one CTA per SM
+constexpr int kSmemPerCta = 227 * 1024;  // one CTA per SM (the sm_103 per-block maximum)
 
 struct Plan {
   int G, S, n_tiles, total, max_pieces, stages, slot_bytes, off_bar;
@@ -998,7 +1065,7 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
     l.x_row = plan.gather ? i * M : 0;
   }
   if (!encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_UINT16, xs_src, w0.K, static_cast<uint64_t>(plan.gather ? n : 1) * M,
-                 static_cast<uint64_t>(w0.K) * 2, kSegsPerStage * 32, M))
+                 static_cast<uint64_t>(w0.K) * 2, kXBox, M))
     return EXQ_ERR_CUDA;
 
   args.counters = reinterpret_cast<uint32_t*>(ws);
@@ -1014,6 +1081,9 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
   args.stages = plan.stages;
   args.slot_bytes = plan.slot_bytes;
   args.off_bar = plan.off_bar;
+  const int starve = testing_starve_rounds();
+  args.wait_limit = starve > 0 ? starve : kWaitLimit;
+  args.starve = starve > 0 ? 1 : 0;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(plan.G, 1, 1);

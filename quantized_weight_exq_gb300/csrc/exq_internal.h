@@ -16,6 +16,10 @@ enum : unsigned {
   kDevErrBadPerm = 4u,      // a permutation entry outside [0, K)
 };
 
+// failure-detection test hook (exq_testing.h): 0 = off, else the wait bound
+// (polling rounds) for launches whose producer is to issue nothing
+int testing_starve_rounds();
+
 struct DeviceInfo {
   int sm_count = 0;
   int max_smem_optin = 0;

@@ -80,6 +80,18 @@ extern "C" int64_t exq_exl2_word_rows(const uint8_t* bits, int32_t n_segments) {
   return total;
 }
 
+// Segment word offsets of an EXL2 layer: the prefix sums of its widths.
+extern "C" exq_status exq_exl2_seg_word_off(const uint8_t* bits, int32_t n_segments, uint32_t* seg_word_off_out) {
+  if (!seg_word_off_out || exq_exl2_word_rows(bits, n_segments) < 0) return EXQ_ERR_INVALID_ARG;
+  uint32_t off = 0;
+  for (int32_t s = 0; s < n_segments; ++s) {
+    seg_word_off_out[s] = off;
+    off += bits[s];
+  }
+  seg_word_off_out[n_segments] = off;
+  return EXQ_OK;
+}
+
 extern "C" exq_status exq_pack_exl2(const uint8_t* q, const uint8_t* bits, int32_t K, int32_t N,
                                     uint32_t* qweight_out, uint32_t* seg_word_off_out) {
   if (!q || !bits || !qweight_out || !seg_word_off_out) return EXQ_ERR_INVALID_ARG;

@@ -29,10 +29,12 @@ EXQ_FMT_EXL2_QSCALE = 3
 
 # every symbol include/exq.h declares
 EXPORTED = (
-    "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_dequant", "exq_gemv_workspace_size",
+    "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_exl2_seg_word_off",
+    "exq_dequant", "exq_gemv_workspace_size",
     "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error", "exq_kv_quantize", "exq_kv_dequantize",
     "exq_quantize_exl2", "exq_measure_exl2_workspace_size", "exq_measure_exl2", "exq_solve_exl2_bits",
+    "exq_testing_starve",
 )
 
 # most layers one exq_gemv_multi call takes (EXQ_GEMV_MAX_LAYERS)
@@ -70,6 +72,7 @@ def _load():
         "exq_pack_exl2": (st, [P, P, i32, i32, P, P]),
         "exq_pack_exl2_qscale": (st, [P, i32, i32, P]),
         "exq_exl2_word_rows": (i64, [P, i32]),
+        "exq_exl2_seg_word_off": (st, [P, i32, P]),
         "exq_dequant": (st, [W, P, P]),
         "exq_gemv_workspace_size": (sz, [W, i32]),
         "exq_gemv": (st, [W, P, i32, P, P, sz, P]),
@@ -86,6 +89,7 @@ def _load():
         "exq_solve_exl2_bits": (st, [P, i32, i64, P]),
         "exq_status_string": (ctypes.c_char_p, [st]),
         "exq_get_last_device_error": (st, [P]),
+        "exq_testing_starve": (None, [i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -145,6 +149,14 @@ def exq_pack_gptq(q: np.ndarray, z: np.ndarray, g_idx: Optional[np.ndarray], gro
 def exq_exl2_word_rows(bits: np.ndarray) -> int:
     bits = np.ascontiguousarray(bits, dtype=np.uint8)
     return int(_lib.exq_exl2_word_rows(_np_ptr(bits), bits.size))
+
+
+def exq_exl2_seg_word_off(bits: np.ndarray) -> np.ndarray:
+    """Segment table uint32 [S + 1] (word-row prefix sums) of the widths [S]."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    off = np.empty(bits.size + 1, dtype=np.uint32)
+    _check(_lib.exq_exl2_seg_word_off(_np_ptr(bits), bits.size, _np_ptr(off)), "exq_exl2_seg_word_off")
+    return off
 
 
 def exq_pack_exl2(q: np.ndarray, bits: np.ndarray):
@@ -383,11 +395,9 @@ def exq_quantize_exl2(W, bits, perm=None, stream=None) -> Weight:
     [K/32] into an EXL2 layer."""
     import torch
     K, N = W.shape
-    bits = np.asarray(bits, dtype=np.int64)
-    off = np.zeros(bits.size + 1, dtype=np.int64)
-    off[1:] = np.cumsum(bits)
+    off = exq_exl2_seg_word_off(bits)
     rows = int(off[-1])
-    off_d = torch.from_numpy(off.astype(np.int32)).to(W.device)
+    off_d = torch.from_numpy(off.view(np.int32)).to(W.device)
     qw = torch.empty(rows, N, dtype=torch.int32, device=W.device)
     sc = torch.empty(K // 32, N, dtype=torch.float16, device=W.device)
     _check(_lib.exq_quantize_exl2(W.data_ptr(), None if perm is None else perm.data_ptr(), K, N, off_d.data_ptr(),
@@ -397,3 +407,10 @@ def exq_quantize_exl2(W, bits, perm=None, stream=None) -> Weight:
 
 def exq_get_last_device_error(stream=None) -> int:
     return int(_lib.exq_get_last_device_error(_stream_ptr(stream)))
+
+
+def exq_testing_starve(wait_rounds: int) -> None:
+    """Failure-detection test hook (include/exq_testing.h): while wait_rounds
+    > 0, GEMV / GEMM launches issue no copies and their bounded waits give up
+    after wait_rounds rounds, so the call ends in EXQ_ERR_TIMEOUT; 0 = off."""
+    _lib.exq_testing_starve(int(wait_rounds))

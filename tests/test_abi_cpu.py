@@ -26,7 +26,7 @@ def exq():
 
 
 def test_library_exports_every_declared_symbol(exq):
-    header = (ROOT / "include" / "exq.h").read_text()
+    header = "\n".join(p.read_text() for p in sorted((ROOT / "include").glob("*.h")))
     header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
     declared = set(re.findall(r"\b(exq_[a-z0-9_]+)\s*\(", header))
     assert declared == set(exq.EXPORTED), declared ^ set(exq.EXPORTED)
@@ -49,6 +49,15 @@ def test_pack_gptq_matches_oracle(exq, act_order, gs):
     assert np.array_equal(perm, operm)
     assert np.array_equal(qw, oqw)
     assert np.array_equal(qz, oqz)
+
+
+def test_exl2_seg_word_off_matches_oracle(exq):
+    bits = np.array([8, 2, 3, 6, 5, 4, 4, 2, 8], dtype=np.uint8)
+    off = exq.exq_exl2_seg_word_off(bits)
+    assert np.array_equal(off, O.exl2_seg_word_off(bits))
+    assert off[0] == 0 and off[-1] == bits.sum()
+    with pytest.raises(exq.ExqError):
+        exq.exq_exl2_seg_word_off(np.array([4, 7], dtype=np.uint8))
 
 
 def test_pack_exl2_matches_oracle(exq):

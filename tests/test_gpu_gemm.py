@@ -134,3 +134,55 @@ def test_prefill_70b_exl2_2p5(env, name):
     W_ref = oracle_W_exl2(e, cols=cols)
     x = synth.activations(512, K, seed=2, workload=wid)
     check_matmul(_gemm(exq, torch, w, x)[:, cols], O.matmul(x, W_ref), f"prefill exl2 {name}")
+
+
+# The prefill sizes the benchmark quotes: the 70B gate shape at M = 2048, and
+# the permuted variants (x gathered pair-interleaved, the XP kernels) at 70B
+# sizes; sampled columns against the oracle, y poisoned with NaN.
+
+def test_prefill_70b_gate_m2048_gptq(env):
+    exq, torch = env
+    K, N = synth.LLAMA2_70B_SHAPES["gate"]
+    wid = synth.WORKLOAD_IDS["prefill_70b"]
+    g = gptq_case(K, N, 128, act_order=False, seed=0, workload=wid, layer=4)
+    cols = _sample_cols(N, n=128, seed=K + 11)
+    x = synth.activations(2048, K, seed=3, workload=wid)
+    y = _gemm(exq, torch, _gptq_dev(exq, g), x)
+    check_matmul(y[:, cols], O.matmul(x, oracle_W_gptq(g, cols=cols)), "prefill gptq gate M=2048")
+
+
+def test_prefill_70b_gate_m2048_exl2_2p5(env):
+    exq, torch = env
+    K, N = synth.LLAMA2_70B_SHAPES["gate"]
+    wid = synth.WORKLOAD_IDS["prefill_70b"]
+    e = exl2_case(K, N, bpw=2.5, allowed=(2, 3, 4), permute=False, seed=0, workload=wid, layer=14)
+    cols = _sample_cols(N, n=128, seed=K + 12)
+    x = synth.activations(2048, K, seed=4, workload=wid)
+    y = _gemm(exq, torch, _exl2_dev(exq, e), x)
+    check_matmul(y[:, cols], O.matmul(x, oracle_W_exl2(e, cols=cols)), "prefill exl2 2.5 gate M=2048")
+
+
+def test_prefill_70b_q_act_order_gptq(env):
+    exq, torch = env
+    K, N = synth.LLAMA2_70B_SHAPES["q"]
+    wid = synth.WORKLOAD_IDS["prefill_70b"]
+    g = gptq_case(K, N, 128, act_order=True, seed=0, workload=wid, layer=20)
+    w = _gptq_dev(exq, g)
+    assert w.perm is not None
+    cols = _sample_cols(N, n=128, seed=K + 13)
+    x = synth.activations(512, K, seed=5, workload=wid)
+    check_matmul(_gemm(exq, torch, w, x)[:, cols], O.matmul(x, oracle_W_gptq(g, cols=cols)),
+                 "prefill gptq act-order q")
+
+
+def test_prefill_70b_down_permuted_exl2_2p5(env):
+    exq, torch = env
+    K, N = synth.LLAMA2_70B_SHAPES["down"]
+    wid = synth.WORKLOAD_IDS["prefill_70b"]
+    e = exl2_case(K, N, bpw=2.5, allowed=(2, 3, 4), permute=True, seed=0, workload=wid, layer=21)
+    w = _exl2_dev(exq, e)
+    assert w.perm is not None
+    cols = _sample_cols(N, n=128, seed=K + 14)
+    x = synth.activations(512, K, seed=6, workload=wid)
+    check_matmul(_gemm(exq, torch, w, x)[:, cols], O.matmul(x, oracle_W_exl2(e, cols=cols)),
+                 "prefill exl2 2.5 permuted down")

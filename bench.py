@@ -86,6 +86,9 @@ def parse_args():
                          "Llama-2-70B gate weight instead (one JSON line)")
     ap.add_argument("--kv-groups", type=int, default=80 * 2 * 32768 * 8,
                     help="groups of 128 values for --kv (default: the whole 70B cache at 32K context)")
+    ap.add_argument("--dequant", action="store_true",
+                    help="time the standalone dequantisation of the 70B gate weight instead (one JSON line)")
+    ap.add_argument("--no-prefill", action="store_true", help="leave the prefill record out of the default line")
     ap.add_argument("--decode-sweep", action="store_true",
                     help="time single GEMVs of the GPTQ 4096, GPTQ act-order 7B and EXL2 4.0 7B workloads "
                          "instead (one JSON line, GB/s per shape and M)")
@@ -234,8 +237,7 @@ def exl2_device_layer(exq, torch, K, N, bits, gen, device, two_level=False, perm
     a bijection, so these are uniform codes), fp16 scales ~ U(0.002, 0.03) or
     two-level scales (uniform 4-bit codes, column maxima ~ U(0.02, 0.05)), and
     a random permutation."""
-    off = np.zeros(bits.size + 1, dtype=np.int64)
-    off[1:] = np.cumsum(bits.astype(np.int64))
+    off = exq.exq_exl2_seg_word_off(bits).astype(np.int64)
     qw = torch.randint(0, 2 ** 32, (int(off[-1]), N), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
     if two_level:
         qs = torch.randint(0, 2 ** 32, (K // 32, N // 8), dtype=torch.int64, device=device,
@@ -326,6 +328,124 @@ def run_prefill(args, device):
         "roofline": {"bound": "tensor", "peak": peak_bf16, "unit": "TFLOPS",
                      "peak_kind": "measured bf16 cuBLAS burst (fp16 runs at the same rate)"},
         "shapes": shapes,
+    }
+
+
+def prefill_record(exq, torch, device, steps: int = 10, warmup: int = 3):
+    """The prefill half of the metric, for the default line: exq_gemm on the
+    Llama-2-70B gate shape (8192 x 28672) at M = 2048, GPTQ g128 and EXL2 2.5
+    bpw; packed words drawn uniformly on the device. CUDA events on the
+    launching stream around `steps` launches after `warmup`; TFLOPS =
+    2 M K N / average launch time, against the measured bf16 burst peak (fp16
+    runs at the same tensor-core rate; each launch is timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_s, kind = float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        peak, peak_s, kind = 1900.0, 1700.0, "fallback"
+    M, (K, N) = 2048, synth.LLAMA2_70B_SHAPES["gate"]
+    out = {"workload": "prefill_70b_gate_8192x28672_M2048", "M": M, "K": K, "N": N, "peak": peak,
+           "peak_kind": f"{kind} bf16 burst (cuBLAS); fp16 runs at the same rate", "unit": "TFLOPS"}
+    stream = torch.cuda.Stream(device=device)
+    for fmt in ("gptq_g128", "exl2_2.5bpw"):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(77 + len(fmt))
+        if fmt.startswith("gptq"):
+            qw = torch.randint(0, 2 ** 32, (K // 8, N), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
+            qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
+                               generator=gen).to(torch.int32)
+            sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
+            w = exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device)
+        else:
+            bits = synth.solve_bit_mix(K // 32, 2.5, (2, 3, 4), np.random.default_rng(K + N))
+            w = exl2_device_layer(exq, torch, K, N, bits, gen, device, perm=False)
+        x = torch.randn(M, K, device=device, generator=gen).half()
+        y = torch.empty(M, N, device=device, dtype=torch.float16)
+        nws = exq.exq_gemm_workspace_size(w, M)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device) if nws else None
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                exq.exq_gemm(w, x, y, ws, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                exq.exq_gemm(w, x, y, ws, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000 / steps
+        tf = 2 * M * K * N / us / 1e6
+        out[fmt] = {"us": round(us, 1), "tflops": round(tf, 1), "frac": round(tf / peak, 4),
+                    "frac_of_sustained": round(tf / peak_s, 4) if peak_s else None,
+                    "kernel": "gemm_kernel (tcgen05, TMEM accumulator)", "launches": steps}
+        del w, x, y, ws
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the prefill record")
+    return out
+
+
+def run_dequant(args, device):
+    """The standalone dequantisation (exq_dequant) of the Llama-2-70B gate
+    weight (8192 x 28672) at EXL2 4.0 bpw (permuted rows), EXL2 4.0 with
+    two-level scales and GPTQ g128: packed words drawn uniformly on the device.
+    CUDA events around `--steps` launches after `--warmup`; GB/s = (packed
+    bytes read + 2 K N bytes written) / time, against the measured HBM copy
+    bandwidth (far above L2: 470 MB written per launch)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_exq_gb300 as exq
+
+    torch.cuda.set_device(device)
+    peak, peak_kind = measured_peaks()
+    K, N = synth.LLAMA2_70B_SHAPES["gate"]
+    res = {}
+    for fmt in ("exl2_4.0bpw", "exl2_4.0bpw_two_level", "gptq_g128"):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(31 + len(fmt))
+        if fmt.startswith("gptq"):
+            qw = torch.randint(0, 2 ** 32, (K // 8, N), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
+            qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
+                               generator=gen).to(torch.int32)
+            sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
+            w = exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device)
+        else:
+            bits = synth.solve_bit_mix(K // 32, 4.0, synth.EXL2_BITS, np.random.default_rng(K))
+            w = exl2_device_layer(exq, torch, K, N, bits, gen, device, two_level=fmt.endswith("two_level"))
+        W = torch.empty(K, N, dtype=torch.float16, device=device)
+        for _ in range(args.warmup):
+            exq.exq_dequant(w, W)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            exq.exq_dequant(w, W)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000 / args.steps
+        moved = w.packed_bytes + 2 * K * N
+        gbs = moved / us / 1e3
+        res[fmt] = {"us": round(us, 1), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "packed_bytes": w.packed_bytes, "written_bytes": 2 * K * N}
+        del w, W
+    if exq.exq_get_last_device_error() != 0:
+        raise RuntimeError("device error word set during the dequant run")
+    return {
+        "metric": "standalone dequant GB/s (packed bytes read + fp16 bytes written)",
+        "value": min(v["GB/s"] for v in res.values()),
+        "unit": UNIT,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "dequant_70b_gate_8192x28672", "value_is": "slowest format",
+                   "l2": "outputs larger than L2 (470 MB of fp16 per launch)"},
+        "roofline": {"bound": "hbm", "peak": peak, "unit": UNIT, "peak_kind": peak_kind},
+        "formats": res,
     }
 
 
@@ -746,21 +866,24 @@ def run_exq(args, rank, world, device):
         "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
+    if not args.no_prefill:
+        result["prefill"] = prefill_record(exq, torch, device)
     return result
 
 
 # ----------------------------------------------------------------------------- oracle
 
-def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 48):
+def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 48, first_layer: int = 0):
     """Time the CPU oracle (as it stands) on a bounded sample of the stream:
-    whole k / v projections (8192 x 1024) of the first layers, packed words
-    drawn exactly as in the GPU stream's recipe (numpy side). Runs in this
-    process with numpy; returns (GB/s of packed bytes, seconds, sample text)."""
+    whole k / v projections (8192 x 1024) of the layers from `first_layer`,
+    packed words drawn exactly as in the GPU stream's recipe (numpy side).
+    Runs in this process with numpy; returns (GB/s of packed bytes, seconds,
+    sample text, bytes)."""
     import oracle as O
 
     wid = synth.WORKLOAD_IDS[WORKLOAD]
     done_bytes, elapsed, n = 0, 0.0, 0
-    layer = 0
+    layer = first_layer
     while n == 0 or (elapsed < seconds_target and n < max_linears):
         for i in (1, 2):  # k, v
             K, N = LINEARS[i][1]
@@ -779,20 +902,61 @@ def oracle_sample_gbs(seconds_target: float = 12.0, max_linears: int = 48):
             if n >= max_linears:
                 break
         layer += 1
-    return done_bytes / elapsed / 1e9, elapsed, f"{n} whole 8192x1024 k/v projections (EXL2 4.0 bpw, M=1)"
+    return done_bytes / elapsed / 1e9, elapsed, f"{n} whole 8192x1024 k/v projections (EXL2 4.0 bpw, M=1)", done_bytes
+
+
+def _oracle_worker(first_layer: int):
+    g, t, _, b = oracle_sample_gbs(seconds_target=6.0, max_linears=24, first_layer=first_layer)
+    return b, t
+
+
+def oracle_parallel_gbs(workers: int):
+    """The same sample split over `workers` processes (spawned: no process of
+    this pool is forked from one that touched a GPU), each on its own layers;
+    GB/s = all bytes / wall time of the pool."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_worker_warm, range(workers))  # interpreters and imports up before the clock
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_worker, [100 + 12 * i for i in range(workers)])
+        wall = time.perf_counter() - t0
+    return sum(b for b, _ in res) / wall / 1e9, wall
+
+
+def _oracle_worker_warm(_):
+    import oracle  # noqa: F401
+    return 0
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def cpu_baseline_subprocess():
-    """Run the oracle timing in a fresh single-threaded process."""
+    """The oracle timing in a fresh process: single-threaded, then one
+    single-threaded process per host core."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cores = os.cpu_count() or 1
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "g, t, s = bench.oracle_sample_gbs(); print(json.dumps([g, t, s]))") % ROOT
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+            "g, t, s, _ = bench.oracle_sample_gbs(); p, w = bench.oracle_parallel_gbs(%d); "
+            "print(json.dumps([g, t, s, p, w]))") % (ROOT, cores)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900, cwd=ROOT)
     if r.returncode != 0:
         return None
-    g, t, s = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": round(g, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{s}; {t:.1f} s of CPU work, numpy float64, single thread"}
+    g, t, s, p, w = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(p, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(), "single_thread_value": round(g, 4),
+            "sample": f"{cores} single-threaded processes, each on whole 8192x1024 k/v projections of its own "
+                      f"layers for about 6 s ({w:.1f} s wall); single thread: {s}, {t:.1f} s; numpy float64"}
 
 
 def run_reference(args):
@@ -802,7 +966,7 @@ def run_reference(args):
         oracle_sample_gbs(seconds_target=0.0, max_linears=1)
     t_total, b_total = 0.0, 0.0
     for _ in range(args.steps):
-        g, t, _ = oracle_sample_gbs(seconds_target=0.0, max_linears=1)
+        g, t, _, _ = oracle_sample_gbs(seconds_target=0.0, max_linears=1)
         t_total += t
         b_total += g * t * 1e9
         res.append(g)
@@ -851,6 +1015,10 @@ def main():
     if args.kv:
         if rank == 0:
             print(json.dumps(run_kv(args, torch.device("cuda", local))), flush=True)
+        return
+    if args.dequant:
+        if rank == 0:
+            print(json.dumps(run_dequant(args, torch.device("cuda", local))), flush=True)
         return
     if args.decode_sweep:
         if rank == 0:

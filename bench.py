@@ -311,6 +311,43 @@ def run_prefill(args, device):
                 tf = 2 * M * K * N / us / 1e6
                 shapes[f"{fmt} M={M} {name} {K}x{N}"] = {"us": round(us, 1), "tflops": round(tf, 1),
                                                           "frac": round(tf / peak_bf16, 4)}
+    # linears that read the same x in one launch (exq_gemm_multi): q+k+v and gate+up
+    for fmt in ("gptq_g128", "exl2_2.5bpw"):
+        for grp in (("q", "k", "v"), ("gate", "up")):
+            for M in ((512, 2048) if grp[0] == "q" else (2048,)):
+                gen = torch.Generator(device=device)
+                gen.manual_seed(2000 * M + len(grp))
+                ws_ = []
+                for name in grp:
+                    K, N = synth.LLAMA2_70B_SHAPES[name]
+                    if fmt.startswith("gptq"):
+                        qw = torch.randint(0, 2 ** 32, (K // 8, N), dtype=torch.int64, device=device,
+                                           generator=gen).to(torch.int32)
+                        qz = torch.randint(0, 2 ** 32, (K // 128, N // 8), dtype=torch.int64, device=device,
+                                           generator=gen).to(torch.int32)
+                        sc = (torch.rand(K // 128, N, device=device, generator=gen) * 0.015 + 0.005).half()
+                        ws_.append(exq.gptq_weight(qw, qz, sc, None, K, N, 128, device=device))
+                    else:
+                        bits = synth.solve_bit_mix(K // 32, 2.5, (2, 3, 4), np.random.default_rng(K + N))
+                        ws_.append(exl2_device_layer(exq, torch, K, N, bits, gen, device, perm=False))
+                K = ws_[0].K
+                x = torch.randn(M, K, device=device, generator=gen).half()
+                ys = [torch.empty(M, w.N, device=device, dtype=torch.float16) for w in ws_]
+                for _ in range(args.warmup):
+                    exq.exq_gemm_multi(ws_, x, ys)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(args.steps):
+                    exq.exq_gemm_multi(ws_, x, ys)
+                e1.record()
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1000 / args.steps
+                ntot = sum(w.N for w in ws_)
+                tf = 2 * M * K * ntot / us / 1e6
+                shapes[f"{fmt} M={M} {'+'.join(grp)} grouped {K}x{ntot}"] = {
+                    "us": round(us, 1), "tflops": round(tf, 1), "frac": round(tf / peak_bf16, 4)}
+                del ws_, x, ys
     if exq.exq_get_last_device_error() != 0:
         raise RuntimeError("device error word set during the prefill sweep")
     best = max(v["tflops"] for v in shapes.values())
@@ -380,6 +417,35 @@ def prefill_record(exq, torch, device, steps: int = 10, warmup: int = 3):
                     "frac_of_sustained": round(tf / peak_s, 4) if peak_s else None,
                     "kernel": "gemm_kernel (tcgen05, TMEM accumulator)", "launches": steps}
         del w, x, y, ws
+    # the q, k and v projections (8192 x 8192, 1024, 1024) in one exq_gemm_multi launch, GPTQ g128
+    gen = torch.Generator(device=device)
+    gen.manual_seed(91)
+    ws_ = []
+    for name in ("q", "k", "v"):
+        Kq, Nq = synth.LLAMA2_70B_SHAPES[name]
+        qw = torch.randint(0, 2 ** 32, (Kq // 8, Nq), dtype=torch.int64, device=device, generator=gen).to(torch.int32)
+        qz = torch.randint(0, 2 ** 32, (Kq // 128, Nq // 8), dtype=torch.int64, device=device,
+                           generator=gen).to(torch.int32)
+        sc = (torch.rand(Kq // 128, Nq, device=device, generator=gen) * 0.015 + 0.005).half()
+        ws_.append(exq.gptq_weight(qw, qz, sc, None, Kq, Nq, 128, device=device))
+    x = torch.randn(M, ws_[0].K, device=device, generator=gen).half()
+    ys = [torch.empty(M, w.N, device=device, dtype=torch.float16) for w in ws_]
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            exq.exq_gemm_multi(ws_, x, ys, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            exq.exq_gemm_multi(ws_, x, ys, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000 / steps
+    ntot = sum(w.N for w in ws_)
+    tf = 2 * M * ws_[0].K * ntot / us / 1e6
+    out["gptq_g128_qkv_grouped"] = {"us": round(us, 1), "tflops": round(tf, 1), "frac": round(tf / peak, 4),
+                                    "shape": f"8192 x (8192 + 1024 + 1024), M = {M}",
+                                    "kernel": "gemm_kernel over the three layers' tiles (exq_gemm_multi)",
+                                    "launches": steps}
     if exq.exq_get_last_device_error() != 0:
         raise RuntimeError("device error word set during the prefill record")
     return out

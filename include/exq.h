@@ -266,6 +266,39 @@ size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M);
 exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* Most layers one exq_gemm_multi call takes. */
+#define EXQ_GEMM_MAX_LAYERS 4
+
+/* Bytes of device workspace exq_gemm_multi needs for these n layers and M:
+ * n * M * K * 2 bytes (rounded up to 256) of activations gathered into each
+ * layer's stored-row order when any of the layers has a permutation, else 0.
+ * Returns 0 also for an invalid group (see exq_gemm_multi). */
+size_t exq_gemm_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M);
+
+/* exq_gemm_multi -- several prefill matmuls that read the same activations,
+ * y_i = x . dequant(Wq_i) for i < n, in ONE launch: the q, k and v
+ * projections of an attention block, or the gate and up projections of an
+ * MLP (the architecture figure of the ExLlamaV2 blog post, section "The
+ * Solution", has the QKV projection as one kernel). The layers stay separate
+ * tensors; their 128-column tiles are pooled in one grid, so a small layer
+ * (the 1024-column k and v of a grouped-query model) shares the GPU with the
+ * large one instead of running alone on a few SMs.
+ *   w  host array of n descriptors, 1 <= n <= EXQ_GEMM_MAX_LAYERS, all of one
+ *      format with the same K and (GPTQ) group size; each N % 128 == 0 and
+ *      K % 64 == 0, else EXQ_ERR_UNSUPPORTED. Permutations may differ.
+ *   x  device fp16 [M, K], input-feature order, shared by every layer
+ *   y  host array of n device pointers, y[i] fp16 [M, w[i].N], fully
+ *      overwritten; they must not overlap one another or x
+ *   workspace  at least exq_gemm_multi_workspace_size() bytes (may be NULL
+ *      when that is 0); scratch; calls that may overlap on the GPU need
+ *      separate workspaces.
+ * No K split: each y[i] has the bits of the unsplit exq_gemm of layer i (a
+ * single exq_gemm of a small layer may split K and then round differently in
+ * the last bit). Deterministic. Returns EXQ_ERR_INVALID_ARG for a bad n,
+ * mixed formats, K or group sizes, a bad pointer or a short workspace. */
+exq_status exq_gemm_multi(const exq_weight* w, int32_t n, const uint16_t* x, int32_t M,
+                          uint16_t* const* y, void* workspace, size_t ws_bytes, void* stream);
+
 /* exq_gemm_noalloc -- exq_gemm for callers that cannot allocate device memory.
  * The ExLlamaV2 pages have no counterpart; this is a deployment variant.
  * Some callers cannot hand the library a workspace: inference-runtime plugins

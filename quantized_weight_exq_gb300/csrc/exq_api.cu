@@ -157,7 +157,28 @@ extern "C" exq_status exq_gemv_multi(const exq_weight* w, int32_t n, const uint1
 
 extern "C" size_t exq_gemm_workspace_size(const exq_weight* w, int32_t M) {
   if (check_weight(w) != EXQ_OK || M < 1) return 0;
-  return gemm_workspace_bytes(*w, M);
+  return gemm_workspace_bytes(w, 1, M);
+}
+
+extern "C" size_t exq_gemm_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M) {
+  if (n > EXQ_GEMM_MAX_LAYERS || check_group(w, n) != EXQ_OK || M < 1) return 0;
+  return gemm_workspace_bytes(w, n, M);
+}
+
+extern "C" exq_status exq_gemm_multi(const exq_weight* w, int32_t n, const uint16_t* x, int32_t M,
+                                     uint16_t* const* y, void* workspace, size_t ws_bytes, void* stream) {
+  if (n > EXQ_GEMM_MAX_LAYERS) return EXQ_ERR_INVALID_ARG;
+  const exq_status st = check_group(w, n);
+  if (st != EXQ_OK) return st;
+  if (!x || !y || !aligned16(x) || M < 1) return EXQ_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!y[i] || !aligned16(y[i])) return EXQ_ERR_INVALID_ARG;
+    if (w[i].K % 64 || w[i].N % 128) return EXQ_ERR_UNSUPPORTED;
+  }
+  const size_t need = gemm_workspace_bytes(w, n, M);
+  if (need && (!workspace || ws_bytes < need || !aligned16(workspace))) return EXQ_ERR_INVALID_ARG;
+  if (current_cc() < 100) return EXQ_ERR_CUDA;
+  return launch_gemm(w, n, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y, void* workspace,
@@ -165,10 +186,10 @@ extern "C" exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M
   const exq_status st = check_weight(w);
   if (st != EXQ_OK) return st;
   if (!x || !y || !aligned16(x) || !aligned16(y) || M < 1) return EXQ_ERR_INVALID_ARG;
-  const size_t need = gemm_workspace_bytes(*w, M);
+  const size_t need = gemm_workspace_bytes(w, 1, M);
   if (need && (!workspace || ws_bytes < need || !aligned16(workspace))) return EXQ_ERR_INVALID_ARG;
   if (current_cc() < 100) return EXQ_ERR_CUDA;
-  return launch_gemm(*w, x, M, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+  return launch_gemm(w, 1, x, M, &y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" exq_status exq_gemm_noalloc(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t* y,

@@ -36,6 +36,8 @@
 // timeout in its device error word, drains its own copies and frees TMEM.
 #include <cuda.h>
 
+#include <algorithm>
+#include <climits>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -90,25 +92,43 @@ constexpr int kMaxSplit = 8;
 constexpr int kMinSlabsPerSplit = 8;
 constexpr int kSplitSmBound = 256;  // SM count the workspace bound allows for
 
+constexpr int kMaxLayers = EXQ_GEMM_MAX_LAYERS;  // layers of one launch (they share x and K)
+
 struct GemmMaps {
-  CUtensorMap x;     // activations [M, K] fp16, boxes 64 x 256, 128-byte swizzle
-  CUtensorMap w;     // qweight [rows, N] uint32, boxes 128 columns x 8 (GPTQ) or 16 (EXL2) rows
-  CUtensorMap s;     // scales [groups, N] fp16, boxes 128 x 1 (unused with two-level scales)
-  CUtensorMap z;     // GPTQ zeros or two-level scale codes [groups, N / 8] uint32, boxes 16 x 1
+  CUtensorMap x;                // activations [rows, K] fp16, boxes 64 x 256, 128-byte swizzle
+  CUtensorMap w[kMaxLayers];    // qweight [rows, N] uint32, boxes 128 columns x 8 (GPTQ) or 16 (EXL2) rows
+  CUtensorMap s[kMaxLayers];    // scales [groups, N] fp16, boxes 128 x 1 (unused with two-level scales)
+  CUtensorMap z[kMaxLayers];    // GPTQ zeros or two-level scale codes [groups, N / 8] uint32, boxes 16 x 1
 };
 
+// One layer of a launch: its column tiles are the grid's y indices
+// tile0 .. (next layer's tile0) - 1; unused entries have tile0 = INT_MAX.
+struct GemmLayer {
+  const uint32_t* seg_off;      // EXL2 [S + 1]
+  const uint16_t* q_scale_max;  // EXL2 two-level column maxima [N]
+  uint16_t* y;                  // [M, N]
+  int N, n_word_rows;
+  int tile0;
+  int x_row;                    // first row of the layer's activations in the x map
+};
 
 struct GemmArgs {
-  const uint32_t* seg_off;
-  const uint16_t* q_scale_max;  // EXL2 two-level column maxima [N]
-  uint16_t* y;
-  float* part;      // [split, M, N] fp32 partial sums when split > 1
-  int M, N, K, gs, n_word_rows;
+  GemmLayer L[kMaxLayers];
+  float* part;      // [split, M, N] fp32 partial sums when split > 1 (one layer only)
+  int M, K, gs;
   int split;        // CTAs along K (gridDim.z)
   int slabs_per;    // 64-row slabs per split (the last split may have fewer)
   int wait_limit;   // polling rounds of a bounded wait (kWaitLimit unless a test lowers it)
   int starve;       // test hook: the producer issues nothing, so the other roles' waits run out
 };
+
+// the layer that owns column tile T (constant indices into the parameters)
+__device__ __forceinline__ int gemm_layer_of(const GemmArgs& a, int T) {
+  int L = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxLayers; ++i) L += T >= a.L[i].tile0 ? 1 : 0;
+  return L;
+}
 
 struct StageMeta {  // written by the producer before the stage's copies
   int rows0, rows1;  // word rows of the two 32-row halves (EXL2 widths; GPTQ 4, 4)
@@ -316,7 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // token tiles vary fastest, so the CTAs that share a column tile's packed
   // weights run together and the repeats come from L2
   const int m0 = blockIdx.x * BT;
-  const int n0 = blockIdx.y * BN;
+  const int layer = gemm_layer_of(a, blockIdx.y);
+  const GemmLayer* ly = &a.L[0] + layer;  // read through the parameter block, no select chain
+  const int n0 = (static_cast<int>(blockIdx.y) - ly->tile0) * BN;
+  const int xm0 = ly->x_row + m0;         // the tile's first row in the x map
   const int kt0 = blockIdx.z * a.slabs_per;                      // this split's first slab
   const int n_iter = min(a.K / BK, kt0 + a.slabs_per) - kt0;     // >= 1 (host plan)
   const int tokens = min(BT, a.M - m0);                          // valid tokens of the tile
@@ -347,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0 && !a.starve) {  // test hook: a starved producer issues nothing
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.x)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.w[0] + layer)) : "memory");
       int issued = 0;
       for (int i = 0; i < n_iter; ++i) {
         const int kt = kt0 + i;
@@ -361,11 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           rows0 = rows1 = 4;
           row_start = kt * 8;
         } else {
-          const unsigned o0 = __ldg(a.seg_off + 2 * kt), o1 = __ldg(a.seg_off + 2 * kt + 1),
-                         o2 = __ldg(a.seg_off + 2 * kt + 2);
+          const unsigned o0 = __ldg(ly->seg_off + 2 * kt), o1 = __ldg(ly->seg_off + 2 * kt + 1),
+                         o2 = __ldg(ly->seg_off + 2 * kt + 2);
           rows0 = static_cast<int>(o1 - o0);
           rows1 = static_cast<int>(o2 - o1);
-          if (!valid_width(rows0) || !valid_width(rows1) || o2 > static_cast<unsigned>(a.n_word_rows) ||
+          if (!valid_width(rows0) || !valid_width(rows1) || o2 > static_cast<unsigned>(ly->n_word_rows) ||
               o1 < o0) {
             atomicOr(&g_gemm_err, kDevErrBadSegment);
             rows0 = rows1 = 0;
@@ -380,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (FMT != EXQ_FMT_EXL2_QSCALE) tx += 2u * BN * 2u;  // fp16 scale rows
         if constexpr (FMT != EXQ_FMT_EXL2) tx += 2u * (BN / 8) * 4u;   // zero or scale-code rows
         mbar_expect_tx(bar, tx);
-        tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, m0, bar);
-        if (rows > 0) tma_load_2d(smem_u32(st + kOffPacked), &maps.w, n0, row_start, bar);
+        tma_load_2d(smem_u32(st + kOffX), &maps.x, kt * BK, xm0, bar);
+        if (rows > 0) tma_load_2d(smem_u32(st + kOffPacked), &maps.w[0] + layer, n0, row_start, bar);
         for (int h = 0; h < 2; ++h) {
           const int g = FMT == EXQ_FMT_GPTQ4 ? (kt * BK + 32 * h) / a.gs : 2 * kt + h;
           if constexpr (FMT != EXQ_FMT_EXL2_QSCALE)
-            tma_load_2d(smem_u32(st + kOffScale + h * BN * 2), &maps.s, n0, g, bar);
+            tma_load_2d(smem_u32(st + kOffScale + h * BN * 2), &maps.s[0] + layer, n0, g, bar);
           if constexpr (FMT != EXQ_FMT_EXL2)
-            tma_load_2d(smem_u32(st + kOffZero + h * kZeroStride), &maps.z, n0 / 8, g, bar);
+            tma_load_2d(smem_u32(st + kOffZero + h * kZeroStride), &maps.z[0] + layer, n0 / 8, g, bar);
         }
         issued = i + 1;
       }
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two-level scales: this column's fp16 maximum, in both halves
     uint32_t m2 = 0u;
     if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) {
-      const uint32_t m = __ldg(a.q_scale_max + n0 + col);
+      const uint32_t m = __ldg(ly->q_scale_max + n0 + col);
       m2 = m | (m << 16);
     }
     for (int i = 0; i < n_iter; ++i) {
@@ -502,15 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + kTmemAcc + t0, r);
         const int mt = tokens - t0;
         if (a.split == 1) {
-          uint16_t* dst = a.y + static_cast<size_t>(m0 + t0) * a.N + n;
+          uint16_t* dst = ly->y + static_cast<size_t>(m0 + t0) * ly->N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < mt) dst[static_cast<size_t>(j) * a.N] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
+            if (j < mt) dst[static_cast<size_t>(j) * ly->N] = __half_as_ushort(__float2half_rn(__uint_as_float(r[j])));
         } else {
-          float* dst = a.part + (static_cast<size_t>(blockIdx.z) * a.M + m0 + t0) * a.N + n;
+          float* dst = a.part + (static_cast<size_t>(blockIdx.z) * a.M + m0 + t0) * ly->N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < mt) dst[static_cast<size_t>(j) * a.N] = __uint_as_float(r[j]);
+            if (j < mt) dst[static_cast<size_t>(j) * ly->N] = __uint_as_float(r[j]);
         }
       }
     }
@@ -550,27 +574,52 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restri
   }
 }
 
-// x_perm[m][j] = x[m][perm[j]]: act-order rows gathered once so the tensor map
-// reads activations in stored-row order
-__global__ void permute_x_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+// x_perm[l][m][j] = x[m][perm_l[j]]: act-order rows gathered once per layer of
+// the launch (grid row l; a layer without a permutation gets a plain copy) so
+// the tensor map reads activations in stored-row order. Entries outside
+// [0, K) read as 0 and are reported.
+struct PermArgs {
+  const int32_t* perm[kMaxLayers];  // NULL: identity
+};
+
+__global__ void permute_x_kernel(const uint16_t* __restrict__ x, const __grid_constant__ PermArgs pa,
                                  uint16_t* __restrict__ xp, int M, int K, bool interleave) {
+  const int l = blockIdx.y;
+  const int32_t* perm = nullptr;
+#pragma unroll
+  for (int i = 0; i < kMaxLayers; ++i)
+    if (l == i) perm = pa.perm[i];
+  uint16_t* out = xp + static_cast<size_t>(l) * M * K;
   const int chunks = K / 8;
   const long long total = static_cast<long long>(M) * chunks;
   for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(e / chunks), c = static_cast<int>(e % chunks);
-    const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c));
-    const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c + 4));
+    int p[8];
+    if (perm) {
+      const int4 p0 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c));
+      const int4 p1 = __ldg(reinterpret_cast<const int4*>(perm + 8 * c + 4));
+      p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
+      p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = 8 * c + i;
+    }
     const uint16_t* xr = x + static_cast<size_t>(m) * K;
-    const uint32_t v0 = __ldg(xr + p0.x), v1 = __ldg(xr + p0.y), v2 = __ldg(xr + p0.z), v3 = __ldg(xr + p0.w);
-    const uint32_t v4 = __ldg(xr + p1.x), v5 = __ldg(xr + p1.y), v6 = __ldg(xr + p1.z), v7 = __ldg(xr + p1.w);
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool ok = static_cast<unsigned>(p[i]) < static_cast<unsigned>(K);
+      if (!ok) atomicOr(&g_gemm_err, kDevErrBadPerm);
+      v[i] = ok ? __ldg(xr + p[i]) : 0u;
+    }
     uint4 o;
     if (interleave) {  // k0 k4 k1 k5 k2 k6 k3 k7
-      o = make_uint4(v0 | (v4 << 16), v1 | (v5 << 16), v2 | (v6 << 16), v3 | (v7 << 16));
+      o = make_uint4(v[0] | (v[4] << 16), v[1] | (v[5] << 16), v[2] | (v[6] << 16), v[3] | (v[7] << 16));
     } else {
-      o = make_uint4(v0 | (v1 << 16), v2 | (v3 << 16), v4 | (v5 << 16), v6 | (v7 << 16));
+      o = make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
     }
-    *reinterpret_cast<uint4*>(xp + static_cast<size_t>(m) * K + 8 * c) = o;
+    *reinterpret_cast<uint4*>(out + static_cast<size_t>(m) * K + 8 * c) = o;
   }
 }
 
@@ -594,8 +643,12 @@ SplitPlan plan_split(int tiles, int slabs, int sms) {
   return {(slabs + per - 1) / per, per};
 }
 
-size_t gather_bytes(const exq_weight& w, int M) {
-  return w.perm ? ((static_cast<size_t>(M) * w.K * 2 + 255) / 256) * 256 : 0;
+// Activations gathered into each layer's stored-row order when any layer of
+// the launch has a permutation: n * M * K * 2 bytes, rounded up to 256.
+size_t gather_bytes(const exq_weight* w, int n, int M) {
+  bool any = false;
+  for (int i = 0; i < n; ++i) any = any || w[i].perm != nullptr;
+  return any ? ((static_cast<size_t>(n) * M * w[0].K * 2 + 255) / 256) * 256 : 0;
 }
 
 size_t partial_bytes(const exq_weight& w, int M, int split) {
@@ -604,122 +657,137 @@ size_t partial_bytes(const exq_weight& w, int M, int split) {
 
 int tiles_of(const exq_weight& w, int M) { return (w.N / BN) * ((M + BT - 1) / BT); }
 
+bool shapes_ok(const exq_weight* w, int n) {
+  for (int i = 0; i < n; ++i)
+    if (w[i].K % BK || w[i].N % BN) return false;
+  return true;
+}
+
+bool encode(EncodeTiled enc, CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+            uint64_t outer, uint64_t stride, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  const cuuint64_t gdim[2] = {inner, outer};
+  const cuuint64_t gstride[1] = {stride};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(map, type, 2, const_cast<void*>(base), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-// Gathered activations (act-order) plus the fp32 partial sums of the largest
-// K split any device up to kSplitSmBound SMs would choose; the launch uses the
-// split of the actual device, which never needs more.
-size_t gemm_workspace_bytes(const exq_weight& w, int M) {
-  size_t bytes = gather_bytes(w, M);
-  if (w.K % BK == 0 && w.N % BN == 0 && M >= 1)
-    bytes += partial_bytes(w, M, plan_split(tiles_of(w, M), w.K / BK, kSplitSmBound).split);
+// Gathered activations (act-order) plus, for a single layer, the fp32 partial
+// sums of the largest K split any device up to kSplitSmBound SMs would choose;
+// the launch uses the split of the actual device, which never needs more.
+// Several layers in one launch never split K (their tiles together fill the GPU).
+size_t gemm_workspace_bytes(const exq_weight* w, int n, int M) {
+  size_t bytes = gather_bytes(w, n, M);
+  if (n == 1 && shapes_ok(w, 1) && M >= 1)
+    bytes += partial_bytes(w[0], M, plan_split(tiles_of(w[0], M), w[0].K / BK, kSplitSmBound).split);
   return bytes;
 }
 
-size_t gemm_gather_bytes(const exq_weight& w, int M) { return gather_bytes(w, M); }
+size_t gemm_gather_bytes(const exq_weight& w, int M) { return gather_bytes(&w, 1, M); }
 
-exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace, size_t ws_bytes,
-                       cudaStream_t stream) {
-  if (w.K % BK || w.N % BN) return EXQ_ERR_UNSUPPORTED;
+exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > kMaxLayers) return EXQ_ERR_INVALID_ARG;
+  if (!shapes_ok(w, n)) return EXQ_ERR_UNSUPPORTED;
   EncodeTiled enc = tensor_map_encoder();
   if (!enc) return EXQ_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
   const int sms = std::min(device_info(dev).sm_count, kSplitSmBound);
+  const exq_weight& w0 = w[0];
 
-  const int slabs = w.K / BK;
-  SplitPlan plan = plan_split(tiles_of(w, M), slabs, sms);
-  const size_t gbytes = gather_bytes(w, M);
-  if (plan.split > 1 && (!workspace || gbytes + partial_bytes(w, M, plan.split) > ws_bytes)) plan = {1, slabs};
+  const int slabs = w0.K / BK;
+  SplitPlan plan{1, slabs};
+  const size_t gbytes = gather_bytes(w, n, M);
+  if (n == 1) {
+    plan = plan_split(tiles_of(w0, M), slabs, sms);
+    if (plan.split > 1 && (!workspace || gbytes + partial_bytes(w0, M, plan.split) > ws_bytes)) plan = {1, slabs};
+  }
   float* part = plan.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gbytes) : nullptr;
 
+  // a permuted layer: x gathered into every layer's stored-row order
+  const bool gather = gbytes > 0;
   const uint16_t* xa = x;
-  if (w.perm) {
+  if (gather) {
     uint16_t* xp = static_cast<uint16_t*>(workspace);
-    const long long total = static_cast<long long>(M) * (w.K / 8);
+    PermArgs pa{};
+    for (int i = 0; i < n; ++i) pa.perm[i] = w[i].perm;
+    const long long total = static_cast<long long>(M) * (w0.K / 8);
     const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4096));
-    permute_x_kernel<<<blocks, 256, 0, stream>>>(x, w.perm, xp, M, w.K, true);
+    permute_x_kernel<<<dim3(blocks, n), 256, 0, stream>>>(x, pa, xp, M, w0.K, true);
     if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
     xa = xp;
   }
 
   GemmMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  const cuuint32_t es[2] = {1, 1};
-  {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.K) * 2};
-    const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(BT)};
-    if (enc(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xa), gdim, gstride, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return EXQ_ERR_CUDA;
-  }
-  {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_word_rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 4};
-    const cuuint32_t box[2] = {BN, static_cast<cuuint32_t>(packed_rows(w.format))};
-    if (enc(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w.qweight), gdim, gstride, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return EXQ_ERR_CUDA;
-  }
-  if (w.scales) {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N), static_cast<cuuint64_t>(w.n_groups)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N) * 2};
-    const cuuint32_t box[2] = {BN, 1};
-    if (enc(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(w.scales), gdim, gstride, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return EXQ_ERR_CUDA;
-  }
-  if (w.format != EXQ_FMT_EXL2) {  // GPTQ zeros or two-level scale codes
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(w.N / 8), static_cast<cuuint64_t>(w.n_groups)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(w.N / 8) * 4};
-    const cuuint32_t box[2] = {BN / 8, 1};
-    const uint32_t* zsrc = w.format == EXQ_FMT_GPTQ4 ? w.qzeros : w.q_scale;
-    if (enc(&maps.z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(zsrc), gdim, gstride, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return EXQ_ERR_CUDA;
-  }
-
+  if (!encode(enc, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xa, w0.K, static_cast<uint64_t>(gather ? n : 1) * M,
+              static_cast<uint64_t>(w0.K) * 2, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B))
+    return EXQ_ERR_CUDA;
   GemmArgs args{};
-  args.seg_off = w.seg_word_off;
-  args.q_scale_max = w.q_scale_max;
-  args.y = y;
+  int tiles = 0;
+  for (int i = 0; i < kMaxLayers; ++i) {
+    GemmLayer& l = args.L[i];
+    if (i >= n) {
+      l.tile0 = INT_MAX;
+      continue;
+    }
+    const exq_weight& wi = w[i];
+    if (!encode(enc, &maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, wi.qweight, wi.N, wi.n_word_rows,
+                static_cast<uint64_t>(wi.N) * 4, BN, packed_rows(wi.format), CU_TENSOR_MAP_SWIZZLE_NONE))
+      return EXQ_ERR_CUDA;
+    if (wi.scales && !encode(enc, &maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, wi.scales, wi.N, wi.n_groups,
+                             static_cast<uint64_t>(wi.N) * 2, BN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return EXQ_ERR_CUDA;
+    if (wi.format != EXQ_FMT_EXL2) {  // GPTQ zeros or two-level scale codes
+      const uint32_t* zsrc = wi.format == EXQ_FMT_GPTQ4 ? wi.qzeros : wi.q_scale;
+      if (!encode(enc, &maps.z[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, zsrc, wi.N / 8, wi.n_groups,
+                  static_cast<uint64_t>(wi.N / 8) * 4, BN / 8, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return EXQ_ERR_CUDA;
+    }
+    l.seg_off = wi.seg_word_off;
+    l.q_scale_max = wi.q_scale_max;
+    l.y = y[i];
+    l.N = wi.N;
+    l.n_word_rows = wi.n_word_rows;
+    l.tile0 = tiles;
+    l.x_row = gather ? i * M : 0;
+    tiles += wi.N / BN;
+  }
   args.part = part;
   args.M = M;
-  args.N = w.N;
-  args.K = w.K;
-  args.gs = w.group_size;
-  args.n_word_rows = w.n_word_rows;
+  args.K = w0.K;
+  args.gs = w0.group_size;
   args.split = plan.split;
   args.slabs_per = plan.slabs_per;
   const int starve = testing_starve_rounds();
   args.wait_limit = starve > 0 ? starve : kWaitLimit;
   args.starve = starve > 0 ? 1 : 0;
 
-  // a permuted layer's x comes from the gather, pair-interleaved
-  const bool xp_mode = w.perm != nullptr;
-  auto fn = w.format == EXQ_FMT_GPTQ4 ? (xp_mode ? gemm_kernel<EXQ_FMT_GPTQ4, true> : gemm_kernel<EXQ_FMT_GPTQ4, false>)
-            : w.format == EXQ_FMT_EXL2
+  // a gathered x is pair-interleaved
+  const bool xp_mode = gather;
+  auto fn = w0.format == EXQ_FMT_GPTQ4
+                ? (xp_mode ? gemm_kernel<EXQ_FMT_GPTQ4, true> : gemm_kernel<EXQ_FMT_GPTQ4, false>)
+            : w0.format == EXQ_FMT_EXL2
                 ? (xp_mode ? gemm_kernel<EXQ_FMT_EXL2, true> : gemm_kernel<EXQ_FMT_EXL2, false>)
                 : (xp_mode ? gemm_kernel<EXQ_FMT_EXL2_QSCALE, true> : gemm_kernel<EXQ_FMT_EXL2_QSCALE, false>);
   static std::once_flag attr_once[6];
-  std::call_once(attr_once[2 * (w.format - 1) + (xp_mode ? 1 : 0)],
+  std::call_once(attr_once[2 * (w0.format - 1) + (xp_mode ? 1 : 0)],
                  [&] { cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
   {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((M + BT - 1) / BT, w.N / BN, plan.split);
+    cfg.gridDim = dim3((M + BT - 1) / BT, tiles, plan.split);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     if (cudaLaunchKernelEx(&cfg, fn, maps, args) != cudaSuccess) return EXQ_ERR_CUDA;
   }
 
-  if (plan.split > 1) {
-    const long long mn = static_cast<long long>(M) * w.N;
+  if (plan.split > 1) {  // one layer
+    const long long mn = static_cast<long long>(M) * w0.N;
     const long long vecs = mn / 8;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(std::min<long long>((vecs + 255) / 256, 8LL * sms)));
@@ -731,7 +799,7 @@ exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(part), y, mn, plan.split) !=
+    if (cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(part), y[0], mn, plan.split) !=
         cudaSuccess)
       return EXQ_ERR_CUDA;
   }
@@ -768,7 +836,7 @@ void* noalloc_scratch(int dev) {
 }  // namespace
 
 exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, cudaStream_t stream) {
-  const size_t need = gather_bytes(w, M);
+  const size_t need = gather_bytes(&w, 1, M);
   if (need > EXQ_NOALLOC_SCRATCH_BYTES) return EXQ_ERR_UNSUPPORTED;
   // the set-up runs on the device's first call whatever the layer, so that a
   // caller who makes one call before stream capture has done it
@@ -776,7 +844,7 @@ exq_status launch_gemm_noalloc(const exq_weight& w, const uint16_t* x, int M, ui
   if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
   void* scratch = noalloc_scratch(dev);
   if (!scratch) return EXQ_ERR_CUDA;
-  return launch_gemm(w, x, M, y, need ? scratch : nullptr, need, stream);
+  return launch_gemm(&w, 1, x, M, &y, need ? scratch : nullptr, need, stream);
 }
 
 unsigned take_gemm_errors(cudaStream_t stream) {

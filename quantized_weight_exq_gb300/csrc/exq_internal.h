@@ -46,9 +46,10 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
                        size_t ws_bytes, cudaStream_t stream);
 size_t gemv_workspace_bytes(const exq_weight* w, int n, int M);
 exq_status launch_dequant(const exq_weight& w, uint16_t* W_out, cudaStream_t stream);
-exq_status launch_gemm(const exq_weight& w, const uint16_t* x, int M, uint16_t* y, void* workspace,
+// n layers (1..EXQ_GEMM_MAX_LAYERS) of one format and K that share x
+exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);
-size_t gemm_workspace_bytes(const exq_weight& w, int M);
+size_t gemm_workspace_bytes(const exq_weight* w, int n, int M);
 // the act-order part of it: M * K * 2 rounded up to 256 bytes, 0 without a permutation
 size_t gemm_gather_bytes(const exq_weight& w, int M);
 // exq_gemm with the library's static scratch array as the workspace

@@ -31,7 +31,7 @@ EXQ_FMT_EXL2_QSCALE = 3
 EXPORTED = (
     "exq_pack_gptq", "exq_pack_exl2", "exq_pack_exl2_qscale", "exq_exl2_word_rows", "exq_exl2_seg_word_off",
     "exq_dequant", "exq_gemv_workspace_size",
-    "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_noalloc", "exq_status_string",
+    "exq_gemv", "exq_gemv_multi_workspace_size", "exq_gemv_multi", "exq_gemm_workspace_size", "exq_gemm", "exq_gemm_multi_workspace_size", "exq_gemm_multi", "exq_gemm_noalloc", "exq_status_string",
     "exq_get_last_device_error", "exq_kv_quantize", "exq_kv_dequantize",
     "exq_quantize_exl2", "exq_measure_exl2_workspace_size", "exq_measure_exl2", "exq_solve_exl2_bits",
     "exq_testing_starve",
@@ -81,6 +81,8 @@ def _load():
         "exq_gemm_workspace_size": (sz, [W, i32]),
         "exq_gemm": (st, [W, P, i32, P, P, sz, P]),
         "exq_gemm_noalloc": (st, [W, P, i32, P, P]),
+        "exq_gemm_multi_workspace_size": (sz, [W, i32, i32]),
+        "exq_gemm_multi": (st, [W, i32, P, i32, P, P, sz, P]),
         "exq_kv_quantize": (st, [P, i64, i32, i32, P, P, P]),
         "exq_kv_dequantize": (st, [P, P, i64, i32, i32, P, P]),
         "exq_quantize_exl2": (st, [P, P, i32, i32, P, i32, P, P, P]),
@@ -330,6 +332,30 @@ def exq_gemm(w: Weight, x, y, workspace=None, stream=None):
     _check(_lib.exq_gemm(ctypes.byref(w.desc()), x.data_ptr(), x.shape[0], y.data_ptr(), ws_ptr, ws_bytes,
                          _stream_ptr(stream)), "exq_gemm")
     return y
+
+
+def exq_gemm_multi_workspace_size(ws, M: int) -> int:
+    return int(_lib.exq_gemm_multi_workspace_size(_desc_array(ws), len(ws), M))
+
+
+def exq_gemm_multi(ws, x, ys, workspace=None, stream=None):
+    """y_i = x . dequant(ws[i]) for the layers ws (one format, one K), in one
+    prefill launch. ``ys`` are the outputs, one per layer."""
+    import torch
+    if len(ws) != len(ys):
+        raise ExqError(EXQ_ERR_INVALID_ARG, "exq_gemm_multi")
+    need = exq_gemm_multi_workspace_size(ws, x.shape[0])
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    yp = (ctypes.c_void_p * len(ys))(*[y.data_ptr() for y in ys])
+    _check(_lib.exq_gemm_multi(_desc_array(ws), len(ws), x.data_ptr(), x.shape[0], yp, ws_ptr, ws_bytes,
+                               _stream_ptr(stream)), "exq_gemm_multi")
+    return ys
+
+
+GEMM_MAX_LAYERS = 4
 
 
 def exq_gemm_noalloc(w: Weight, x, y, stream=None):

@@ -271,8 +271,10 @@ exq_status exq_gemm(const exq_weight* w, const uint16_t* x, int32_t M, uint16_t*
 
 /* Bytes of device workspace exq_gemm_multi needs for these n layers and M:
  * n * M * K * 2 bytes (rounded up to 256) of activations gathered into each
- * layer's stored-row order when any of the layers has a permutation, else 0.
- * Returns 0 also for an invalid group (see exq_gemm_multi). */
+ * layer's stored-row order when any of the layers has a permutation, plus
+ * the fp32 partial sums of the largest K split that any one of the layers
+ * would take alone (as in exq_gemm_workspace_size). 0 when neither applies,
+ * and for an invalid group (see exq_gemm_multi). */
 size_t exq_gemm_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M);
 
 /* exq_gemm_multi -- several prefill matmuls that read the same activations,
@@ -292,10 +294,14 @@ size_t exq_gemm_multi_workspace_size(const exq_weight* w, int32_t n, int32_t M);
  *   workspace  at least exq_gemm_multi_workspace_size() bytes (may be NULL
  *      when that is 0); scratch; calls that may overlap on the GPU need
  *      separate workspaces.
- * No K split: each y[i] has the bits of the unsplit exq_gemm of layer i (a
- * single exq_gemm of a small layer may split K and then round differently in
- * the last bit). Deterministic. Returns EXQ_ERR_INVALID_ARG for a bad n,
- * mixed formats, K or group sizes, a bad pointer or a short workspace. */
+ * The call picks, from the shapes and the device's SM count, one launch over
+ * the pooled tiles or one launch per layer, whichever fills the SMs in fewer
+ * waves (one launch per layer splits K for a small layer as exq_gemm does);
+ * x is gathered once either way. Each y[i] has the bits of exq_gemm on
+ * layer i, or of its unsplit form when exq_gemm would split K and the group
+ * is pooled (they differ at most in the last bit). Deterministic for given
+ * shapes and device. Returns EXQ_ERR_INVALID_ARG for a bad n, mixed formats,
+ * K or group sizes, a bad pointer or a short workspace. */
 exq_status exq_gemm_multi(const exq_weight* w, int32_t n, const uint16_t* x, int32_t M,
                           uint16_t* const* y, void* workspace, size_t ws_bytes, void* stream);
 

@@ -675,56 +675,72 @@ bool encode(EncodeTiled enc, CUtensorMap* map, CUtensorMapDataType type, const v
 
 }  // namespace
 
-// Gathered activations (act-order) plus, for a single layer, the fp32 partial
-// sums of the largest K split any device up to kSplitSmBound SMs would choose;
-// the launch uses the split of the actual device, which never needs more.
-// Several layers in one launch never split K (their tiles together fill the GPU).
+namespace {
+
+// Waves of one K-deep tile each (in units of one unsplit tile's time) that a
+// launch of `tiles` CTAs split `split` ways along K takes on `sms` SMs: the
+// CTAs are not persistent, so a partial last wave costs a whole one.
+double launch_waves(int tiles, int split, int sms) {
+  return static_cast<double>((static_cast<long long>(tiles) * split + sms - 1) / sms) / split;
+}
+
+// What a launch costs beyond its waves (start-up, pipeline fill, the K-split
+// reduction), in the same units; ties go to fewer launches.
+constexpr double kLaunchWaves = 0.15;
+
+// The K split each layer of a group would take alone, within the workspace
+// left after the gathered activations.
+SplitPlan layer_plan(const exq_weight& w, int M, int sms, size_t room) {
+  SplitPlan p = plan_split(tiles_of(w, M), w.K / BK, sms);
+  if (p.split > 1 && partial_bytes(w, M, p.split) > room) p = {1, w.K / BK};
+  return p;
+}
+
+// A group runs as one launch over its pooled tiles unless one launch per
+// layer (each split as exq_gemm would split it) fills the SMs in fewer waves:
+// q + k + v of a 70B model at M = 512 pools 160 tiles, two waves on 152 SMs,
+// where q alone is one wave and k, v each an eighth of one split eight ways.
+bool pool_layers(const exq_weight* w, int n, int M, int sms, size_t room) {
+  if (n == 1) return false;
+  int pooled = 0;
+  double apart = kLaunchWaves * (n - 1);
+  for (int i = 0; i < n; ++i) {
+    pooled += tiles_of(w[i], M);
+    const SplitPlan p = layer_plan(w[i], M, sms, room);
+    apart += launch_waves(tiles_of(w[i], M), p.split, sms) + (p.split > 1 ? kLaunchWaves : 0.0);
+  }
+  return launch_waves(pooled, 1, sms) <= apart;
+}
+
+}  // namespace
+
+// Gathered activations (act-order) plus the fp32 partial sums of the largest
+// K split that any layer of the group takes alone on a device of up to
+// kSplitSmBound SMs (layers launched one by one reuse one partial buffer);
+// the launch plans for the actual device, which never needs more.
 size_t gemm_workspace_bytes(const exq_weight* w, int n, int M) {
-  size_t bytes = gather_bytes(w, n, M);
-  if (n == 1 && shapes_ok(w, 1) && M >= 1)
-    bytes += partial_bytes(w[0], M, plan_split(tiles_of(w[0], M), w[0].K / BK, kSplitSmBound).split);
-  return bytes;
+  size_t bytes = gather_bytes(w, n, M), part = 0;
+  if (shapes_ok(w, n) && M >= 1)
+    for (int i = 0; i < n; ++i)
+      part = std::max(part, partial_bytes(w[i], M, plan_split(tiles_of(w[i], M), w[i].K / BK, kSplitSmBound).split));
+  return bytes + part;
 }
 
 size_t gemm_gather_bytes(const exq_weight& w, int M) { return gather_bytes(&w, 1, M); }
 
-exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
-                       size_t ws_bytes, cudaStream_t stream) {
-  if (n < 1 || n > kMaxLayers) return EXQ_ERR_INVALID_ARG;
-  if (!shapes_ok(w, n)) return EXQ_ERR_UNSUPPORTED;
-  EncodeTiled enc = tensor_map_encoder();
-  if (!enc) return EXQ_ERR_CUDA;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
-  const int sms = std::min(device_info(dev).sm_count, kSplitSmBound);
+namespace {
+
+// One gemm_kernel launch over the pooled column tiles of layers w[0, n),
+// reading x rows [x_row_i, x_row_i + M) of the [x_rows, K] activations `xa`
+// (pair-interleaved when `xp_mode`); with plan.split > 1 (n == 1 only) the
+// fp32 partials go to `part` and a reduction kernel writes y[0].
+exq_status launch_tiles(EncodeTiled enc, const exq_weight* w, int n, const uint16_t* xa, bool xp_mode,
+                        int x_rows, bool stacked, int M, uint16_t* const* y, SplitPlan plan, float* part, int sms,
+                        cudaStream_t stream) {
   const exq_weight& w0 = w[0];
-
-  const int slabs = w0.K / BK;
-  SplitPlan plan{1, slabs};
-  const size_t gbytes = gather_bytes(w, n, M);
-  if (n == 1) {
-    plan = plan_split(tiles_of(w0, M), slabs, sms);
-    if (plan.split > 1 && (!workspace || gbytes + partial_bytes(w0, M, plan.split) > ws_bytes)) plan = {1, slabs};
-  }
-  float* part = plan.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gbytes) : nullptr;
-
-  // a permuted layer: x gathered into every layer's stored-row order
-  const bool gather = gbytes > 0;
-  const uint16_t* xa = x;
-  if (gather) {
-    uint16_t* xp = static_cast<uint16_t*>(workspace);
-    PermArgs pa{};
-    for (int i = 0; i < n; ++i) pa.perm[i] = w[i].perm;
-    const long long total = static_cast<long long>(M) * (w0.K / 8);
-    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4096));
-    permute_x_kernel<<<dim3(blocks, n), 256, 0, stream>>>(x, pa, xp, M, w0.K, true);
-    if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
-    xa = xp;
-  }
-
   GemmMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (!encode(enc, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xa, w0.K, static_cast<uint64_t>(gather ? n : 1) * M,
+  if (!encode(enc, &maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xa, w0.K, static_cast<uint64_t>(x_rows),
               static_cast<uint64_t>(w0.K) * 2, BK, BT, CU_TENSOR_MAP_SWIZZLE_128B))
     return EXQ_ERR_CUDA;
   GemmArgs args{};
@@ -754,7 +770,7 @@ exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uin
     l.N = wi.N;
     l.n_word_rows = wi.n_word_rows;
     l.tile0 = tiles;
-    l.x_row = gather ? i * M : 0;
+    l.x_row = stacked ? i * M : 0;
     tiles += wi.N / BN;
   }
   args.part = part;
@@ -767,8 +783,6 @@ exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uin
   args.wait_limit = starve > 0 ? starve : kWaitLimit;
   args.starve = starve > 0 ? 1 : 0;
 
-  // a gathered x is pair-interleaved
-  const bool xp_mode = gather;
   auto fn = w0.format == EXQ_FMT_GPTQ4
                 ? (xp_mode ? gemm_kernel<EXQ_FMT_GPTQ4, true> : gemm_kernel<EXQ_FMT_GPTQ4, false>)
             : w0.format == EXQ_FMT_EXL2
@@ -802,6 +816,51 @@ exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uin
     if (cudaLaunchKernelEx(&cfg, split_reduce_kernel, static_cast<const float*>(part), y[0], mn, plan.split) !=
         cudaSuccess)
       return EXQ_ERR_CUDA;
+  }
+  return EXQ_OK;
+}
+
+}  // namespace
+
+exq_status launch_gemm(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (n < 1 || n > kMaxLayers) return EXQ_ERR_INVALID_ARG;
+  if (!shapes_ok(w, n)) return EXQ_ERR_UNSUPPORTED;
+  EncodeTiled enc = tensor_map_encoder();
+  if (!enc) return EXQ_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return EXQ_ERR_CUDA;
+  const int sms = std::min(device_info(dev).sm_count, kSplitSmBound);
+  const int K = w[0].K;
+
+  const size_t gbytes = gather_bytes(w, n, M);
+  const size_t room = workspace && ws_bytes > gbytes ? ws_bytes - gbytes : 0;
+  float* part = room ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gbytes) : nullptr;
+
+  // a permuted layer: x gathered once into every layer's stored-row order,
+  // layer i's copy at rows [i * M, (i + 1) * M), pair-interleaved
+  const bool gather = gbytes > 0;
+  const uint16_t* xa = x;
+  if (gather) {
+    uint16_t* xp = static_cast<uint16_t*>(workspace);
+    PermArgs pa{};
+    for (int i = 0; i < n; ++i) pa.perm[i] = w[i].perm;
+    const long long total = static_cast<long long>(M) * (K / 8);
+    const int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 4096));
+    permute_x_kernel<<<dim3(blocks, n), 256, 0, stream>>>(x, pa, xp, M, K, true);
+    if (cudaGetLastError() != cudaSuccess) return EXQ_ERR_CUDA;
+    xa = xp;
+  }
+
+  if (pool_layers(w, n, M, sms, room))
+    return launch_tiles(enc, w, n, xa, gather, gather ? n * M : M, gather, M, y, SplitPlan{1, K / BK}, nullptr, sms,
+                        stream);
+  for (int i = 0; i < n; ++i) {
+    const SplitPlan p = layer_plan(w[i], M, sms, room);
+    const uint16_t* xi = gather ? xa + static_cast<size_t>(i) * M * K : x;
+    const exq_status st = launch_tiles(enc, w + i, 1, xi, gather, M, false, M, y + i, p, p.split > 1 ? part : nullptr,
+                                       sms, stream);
+    if (st != EXQ_OK) return st;
   }
   return EXQ_OK;
 }

@@ -89,6 +89,32 @@ def test_gemm_multi_matches_unsplit_single_calls(env):
         assert np.array_equal(y1.float().cpu().numpy().astype(np.float64), y)
 
 
+def test_gemm_multi_per_layer_launches_match_single_calls(env):
+    exq, torch = env
+    # q + k + v shaped like a grouped-query block at M = 512: pooled, the 160
+    # tiles would take two waves on 152 SMs, so the call launches per layer
+    # and splits the small layers along K as exq_gemm does; the permuted
+    # layers read their own slice of the once-gathered activations
+    K, M = 4096, 512
+    es = [exl2_case(K, 8192, bpw=4.0, seed=71), exl2_case(K, 1024, bpw=4.0, permute=False, seed=72),
+          exl2_case(K, 1024, bpw=3.0, allowed=(2, 3, 4), seed=73)]
+    ws = [_exl2_dev(exq, e) for e in es]
+    x16 = synth.activations(M, K, seed=70)
+    ys = _multi(exq, torch, ws, x16)
+    x = torch.from_numpy(x16).cuda()
+    per_layer = torch.cuda.get_device_properties(0).multi_processor_count == 152
+    rng = np.random.default_rng(70)
+    for i, (e, w, y) in enumerate(zip(es, ws, ys)):
+        cols = np.unique(np.concatenate([rng.choice(w.N, 64, replace=False), [0, w.N - 1]]))
+        check_matmul(y[:, cols], O.matmul(x16, oracle_W_exl2(e, cols=cols)), f"multi per-layer {i}")
+        y1 = torch.full((M, w.N), float("nan"), dtype=torch.float16, device="cuda")
+        wsb = torch.empty(max(exq.exq_gemm_workspace_size(w, M), 16), dtype=torch.uint8, device="cuda")
+        exq.exq_gemm(w, x, y1, wsb)
+        torch.cuda.synchronize()
+        if per_layer or i == 0:  # q alone never splits K at M = 512
+            assert np.array_equal(y1.float().cpu().numpy().astype(np.float64), y), f"layer {i}"
+
+
 def test_gemm_multi_qkv_70b(env):
     exq, torch = env
     # the Llama-2-70B q, k, v projections at M = 512, act-order GPTQ, one launch

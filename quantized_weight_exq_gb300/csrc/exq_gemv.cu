@@ -176,9 +176,10 @@ __device__ __forceinline__ GemvLayer layer_params(const GemvArgs& a, int L) {
 //   wlo, whi: EXL2 widths, 4 bits per segment (segments 0-7, 8-15; 0 = skip)
 //   c: tile (global over the launch's layers) | layer << 16
 //   gpos: GPTQ: position in its group of the stage's first segment
+//   seq: the stage's index in the CTA's sequence (see stage_wait)
 struct Desc {
   uint32_t a, wlo, whi, c;
-  uint32_t gpos, pad0, pad1, pad2;
+  uint32_t gpos, seq, pad1, pad2;
 };
 constexpr uint32_t kDescLast = 1u << 8;     // after this stage the set flushes its partial sums
 constexpr uint32_t kDescEnd = 1u << 9;      // no more stages for this set
@@ -222,6 +223,32 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   for (int i = 0; i < limit; ++i) {
     int state = 0;  // 1 = phase complete, 2 = another role gave up
     if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state == 1) return true;
+    if (state == 2) return false;
+  }
+  if (leader) {
+    atomicOr(&g_gemv_err, kDevErrTimeout);
+    *abort_flag = 1;
+  }
+  return false;
+}
+
+// The wait of a consumer set for stage j of its slot. Both sets use every
+// slot in turn, so a set's successive stages in one slot are two phases of
+// its full barrier apart, and a parity wait alone also passes while the
+// barrier is still short of the other set's stage in between (same parity
+// two phases back). The descriptor closes that gap: the producer writes
+// stage j's descriptor, with seq = j, only after the slot's previous stage
+// was released, hence after it landed; once the descriptor shows j, the
+// barrier is at stage j or past it and the parity wait is exact.
+__device__ __forceinline__ bool stage_wait(const uint32_t* seq, uint32_t j, uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag, int limit) {
+  const bool leader = (threadIdx.x & 31) == 0;
+  const volatile uint32_t* vseq = seq;
+  for (int i = 0; i < limit; ++i) {
+    int state = 0;  // 1 = stage j landed, 2 = another role gave up
+    if (leader) state = (*vseq == j && mbar_try_wait(bar, parity)) ? 1 : (*abort_flag ? 2 : 0);
     state = __shfl_sync(0xffffffffu, state, 0);
     if (state == 1) return true;
     if (state == 2) return false;
@@ -537,6 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), kColGroups);  // the eight warps of the stage's set read it
+      desc[i].seq = ~0u;                            // no stage yet
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -614,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t fb = smem_u32(&full[slot]);
       if (lane == 0)
         desc[slot] = Desc{da, wlo, whi, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16), gpos,
-                          0u, 0u, 0u};
+                          static_cast<uint32_t>(issued), 0u, 0u};
       const int nx = n > kGptqSegs ? 2 : 1;
       if constexpr (FMT != EXQ_FMT_EXL2) {
         if (!bad) {
@@ -651,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waited && issued >= a.stages) release_x();
       if (!warp_wait(smem_u32(&empty[slot]), ephase ^ 1, abort_flag, a.wait_limit)) return false;
       if (lane == 0) {
-        desc[slot] = Desc{da, 0u, 0u, dc, 0u, 0u, 0u, 0u};
+        desc[slot] = Desc{da, 0u, 0u, dc, 0u, static_cast<uint32_t>(issued), 0u, 0u};
         mbar_arrive(smem_u32(&full[slot]));
       }
       next_slot();
@@ -753,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Acc<MT> acc;
   zero_acc<MT>(acc);
   int slot = set, fphase = 0;  // this set's first stage (stages >= 2)
-  for (;;) {
-    if (!warp_wait(smem_u32(&full[slot]), fphase, abort_flag, a.wait_limit)) break;
+  for (uint32_t j = static_cast<uint32_t>(set);; j += kSets) {
+    if (!stage_wait(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag, a.wait_limit)) break;
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
     const uint8_t* sl = smem + slot * a.slot_bytes;

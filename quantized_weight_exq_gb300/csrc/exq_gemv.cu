@@ -91,10 +91,15 @@ constexpr int kRowsPerStage = 32;        // packed word rows per stage (box heig
 constexpr int kScaleRows = 16;           // scale (and GPTQ zero) rows per stage
 constexpr int kCounterBytes = 64 * 1024; // workspace counter region (zero between calls)
 constexpr int kMaxStages = 6;
-// try_wait rounds before giving up. A round without a suspend hint returns
-// after a short, hardware-chosen time; polling this way measured 1.4 % faster
-// on the 70B stream than sleeping with a 20 us hint (the waking is slower).
+// try_wait rounds before giving up. The producer polls (a round without a
+// suspend hint returns after a short, hardware-chosen time): it must issue
+// the next copy as soon as a slot frees. Consumers sleep in the wait, up to
+// kWaitHintNs a round, so that a set waiting for data does not take issue
+// slots from the set that is computing (1.2 % faster on the 70B stream than
+// polling consumers).
 constexpr int kWaitLimit = 1 << 24;
+constexpr int kSleepLimit = 1 << 17;       // consumer rounds: at most 2.6 s
+constexpr uint32_t kWaitHintNs = 20000;
 
 // slot layout (bytes): word rows | scale rows | GPTQ zero rows | x [2][M][256]
 constexpr int kRowBytes = kTN * 4;                         // 992
@@ -152,6 +157,7 @@ struct GemvArgs {
   int slot_bytes;
   int off_bar;              // byte offset of the barriers, descriptors and tables
   int wait_limit;           // polling rounds of a bounded wait (kWaitLimit unless a test lowers it)
+  int sleep_limit;          // sleeping rounds of a consumer's wait (kSleepLimit unless a test lowers it)
   int starve;               // test hook: the producer issues nothing, so the consumers' waits run out
 };
 
@@ -215,6 +221,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread until the phase completes, at most
+// kWaitHintNs
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait by lane 0 of a warp, result broadcast to the warp (all lanes
 // leave in the same round). A timeout is recorded and raises the abort flag;
 // a raised flag makes every other waiter give up too.
@@ -248,7 +268,7 @@ __device__ __forceinline__ bool stage_wait(const uint32_t* seq, uint32_t j, uint
   const volatile uint32_t* vseq = seq;
   for (int i = 0; i < limit; ++i) {
     int state = 0;  // 1 = stage j landed, 2 = another role gave up
-    if (leader) state = (*vseq == j && mbar_try_wait(bar, parity)) ? 1 : (*abort_flag ? 2 : 0);
+    if (leader) state = (*vseq == j && mbar_try_wait_sleep(bar, parity)) ? 1 : (*abort_flag ? 2 : 0);
     state = __shfl_sync(0xffffffffu, state, 0);
     if (state == 1) return true;
     if (state == 2) return false;
@@ -348,27 +368,40 @@ __device__ __forceinline__ void exl2_unpack(const uint8_t* row, uint32_t off, ui
   }
 }
 
-// The lane's four column scales, each in both halves of a word, from one
-// 8-byte read of a scale row.
+// The lane's four column scales from one 8-byte read of a scale row: s2[c]
+// is the word that holds column c's scale, in its low half for even c and
+// its high half for odd c (scale_pairs broadcasts the half it needs).
 __device__ __forceinline__ void scales4(const uint8_t* p, uint32_t (&s2)[4]) {
   const uint2 v = lds64(p);
-  s2[0] = prmt(v.x, v.x, 0x1010);
-  s2[1] = prmt(v.x, v.x, 0x3232);
-  s2[2] = prmt(v.y, v.y, 0x1010);
-  s2[3] = prmt(v.y, v.y, 0x3232);
+  s2[0] = s2[1] = v.x;
+  s2[2] = s2[3] = v.y;
 }
 
 // two-level scales: the exact fractions (c + 1) / 16 of the lane's four
-// columns, each in both halves of a word; `codes` = their 4-bit codes in the
+// columns, laid out like scales4's words; `codes` = their 4-bit codes in the
 // low 16 bits
 __device__ __forceinline__ void qfracs4(uint32_t codes, uint32_t (&s2)[4]) {
   const uint32_t lo = codes & 0xFFFFu, hi = lo >> 8;
-  const uint32_t a = two_level_frac2(lo | (lo << 12));  // columns 0, 1
-  const uint32_t b = two_level_frac2(hi | (hi << 12));  // columns 2, 3
-  s2[0] = prmt(a, a, 0x1010);
-  s2[1] = prmt(a, a, 0x3232);
-  s2[2] = prmt(b, b, 0x1010);
-  s2[3] = prmt(b, b, 0x3232);
+  s2[0] = s2[1] = two_level_frac2(lo | (lo << 12));  // columns 0, 1
+  s2[2] = s2[3] = two_level_frac2(hi | (hi << 12));  // columns 2, 3
+}
+
+__device__ __forceinline__ __half2 as_h2(uint32_t v) {
+  __half2 h;
+  memcpy(&h, &v, 4);
+  return h;
+}
+__device__ __forceinline__ uint32_t as_u32(__half2 h) {
+  uint32_t v;
+  memcpy(&v, &h, 4);
+  return v;
+}
+
+// column c's half of a scales4 / qfracs4 word in both halves: written with
+// the half2 intrinsics, so that the compiler can take the half as an
+// operand of the multiply instead of a separate permute
+__device__ __forceinline__ __half2 col_half(uint32_t w, int c) {
+  return (c & 1) ? __high2half2(as_h2(w)) : __low2half2(as_h2(w));
 }
 
 // w = fp16_RN((q - z) s) for the lane's four columns: one fp16 multiply per
@@ -378,12 +411,15 @@ __device__ __forceinline__ void qfracs4(uint32_t codes, uint32_t (&s2)[4]) {
 template <int FMT>
 __device__ __forceinline__ void scale_pairs(uint32_t (&P)[4][4], const uint32_t (&s2)[4], const uint32_t (&m2)[4]) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 4; ++c) {
+    const __half2 s = col_half(s2[c], c);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      P[c][i] = hmul2(P[c][i], s2[c]);
-      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) P[c][i] = hmul2(P[c][i], m2[c]);
+      __half2 w = __hmul2_rn(as_h2(P[c][i]), s);
+      if constexpr (FMT == EXQ_FMT_EXL2_QSCALE) w = __hmul2_rn(w, col_half(m2[c], c));
+      P[c][i] = as_u32(w);
     }
+  }
 }
 
 template <int MT>
@@ -782,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   zero_acc<MT>(acc);
   int slot = set, fphase = 0;  // this set's first stage (stages >= 2)
   for (uint32_t j = static_cast<uint32_t>(set);; j += kSets) {
-    if (!stage_wait(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag, a.wait_limit)) break;
+    if (!stage_wait(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag, a.sleep_limit)) break;
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
     const uint8_t* sl = smem + slot * a.slot_bytes;
@@ -1111,6 +1147,7 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
   args.off_bar = plan.off_bar;
   const int starve = testing_starve_rounds();
   args.wait_limit = starve > 0 ? starve : kWaitLimit;
+  args.sleep_limit = starve > 0 ? starve : kSleepLimit;
   args.starve = starve > 0 ? 1 : 0;
 
   cudaLaunchConfig_t cfg{};

@@ -549,31 +549,44 @@ __device__ __forceinline__ void run_uniform(const uint8_t* wp, const uint8_t* sp
   }
 }
 
+// One EXL2 segment of width B, whole: its activations and scales, unpack,
+// scale, multiply. Each width of a mixed stage runs its own copy of all of
+// it, so that nothing after the width dispatch has to merge the per-width
+// values into common registers.
+template <int FMT, int B, int MT, bool XP>
+__device__ __forceinline__ void exl2_segment(const uint8_t* row, const uint8_t* sp, const uint8_t* xp, int dx, int t,
+                                             const uint32_t (&m2)[4], const uint8_t* cp, int csh, Acc<MT>& acc) {
+  uint32_t xb[MT][4], s2[4], P[4][4];
+  load_x<MT, XP>(xp, dx, xb);
+  if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+    qfracs4(lds32(cp) >> csh, s2);
+  else
+    scales4(sp, s2);
+  exl2_unpack<B>(row + blk_row_bytes<B>(t), blk_bit<B>(t), P);
+  scale_pairs<FMT>(P, s2, m2);
+  seg_mma<MT>(acc, P, xb);
+}
+
 // EXL2, widths from the descriptor (4 bits per segment): n segments of one x
-// box; returns the word row after them
+// box; returns the word row after them. Width 0 is a segment the producer
+// rejected (reported): it takes no rows.
 template <int FMT, int MT, bool XP>
 __device__ __forceinline__ const uint8_t* run_mixed(const uint8_t* row, const uint8_t* sp, const uint8_t* xp, int dx,
                                                     int t, int n, uint32_t widths, const uint32_t (&m2)[4],
                                                     const uint8_t* cp, int csh, Acc<MT>& acc) {
   for (int j = 0; j < n; ++j, widths >>= 4) {
-    const int b = static_cast<int>(widths & 15u);
-    if (b == 0) continue;  // a segment the producer rejected (reported); it takes no rows
-    uint32_t xb[MT][4], s2[4], P[4][4];
-    load_x<MT, XP>(xp + 64 * j, dx, xb);
-    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
-      qfracs4(lds32(cp + j * kZeroRowBytes) >> csh, s2);
-    else
-      scales4(sp + j * kScaleRowBytes, s2);
-    switch (b) {
-      case 2: exl2_unpack<2>(row + blk_row_bytes<2>(t), blk_bit<2>(t), P); row += 2 * kRowBytes; break;
-      case 3: exl2_unpack<3>(row + blk_row_bytes<3>(t), blk_bit<3>(t), P); row += 3 * kRowBytes; break;
-      case 4: exl2_unpack<4>(row + blk_row_bytes<4>(t), blk_bit<4>(t), P); row += 4 * kRowBytes; break;
-      case 5: exl2_unpack<5>(row + blk_row_bytes<5>(t), blk_bit<5>(t), P); row += 5 * kRowBytes; break;
-      case 6: exl2_unpack<6>(row + blk_row_bytes<6>(t), blk_bit<6>(t), P); row += 6 * kRowBytes; break;
-      default: exl2_unpack<8>(row + blk_row_bytes<8>(t), blk_bit<8>(t), P); row += 8 * kRowBytes; break;
+    const uint8_t* sj = sp + j * kScaleRowBytes;
+    const uint8_t* xj = xp + 64 * j;
+    const uint8_t* cj = cp + j * kZeroRowBytes;
+    switch (widths & 15u) {
+      case 2: exl2_segment<FMT, 2, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 2 * kRowBytes; break;
+      case 3: exl2_segment<FMT, 3, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 3 * kRowBytes; break;
+      case 4: exl2_segment<FMT, 4, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 4 * kRowBytes; break;
+      case 5: exl2_segment<FMT, 5, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 5 * kRowBytes; break;
+      case 6: exl2_segment<FMT, 6, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 6 * kRowBytes; break;
+      case 8: exl2_segment<FMT, 8, MT, XP>(row, sj, xj, dx, t, m2, cj, csh, acc); row += 8 * kRowBytes; break;
+      default: break;
     }
-    scale_pairs<FMT>(P, s2, m2);
-    seg_mma<MT>(acc, P, xb);
   }
   return row;
 }

@@ -549,6 +549,29 @@ __device__ __forceinline__ void run_uniform(const uint8_t* wp, const uint8_t* sp
   }
 }
 
+// EXL2, a whole stage of width B (32 / B segments, at most 16): the loop
+// runs a compile-time count, so every address is an immediate offset
+template <int FMT, int B, int MT, bool XP>
+__device__ __forceinline__ void run_full(const uint8_t* wp, const uint8_t* sp, const uint8_t* xp, int xbox, int dx,
+                                         int t, const uint32_t (&m2)[4], const uint8_t* cp, int csh, Acc<MT>& acc) {
+  constexpr int kN = (32 / B) < 16 ? 32 / B : 16;
+  const uint8_t* wrow = wp + blk_row_bytes<B>(t);
+  const uint32_t off = blk_bit<B>(t);
+  const uint8_t* xq = xp + xbox - 64 * kGptqSegs;  // segments 8.. read the second x box
+#pragma unroll
+  for (int j = 0; j < kN; ++j) {
+    uint32_t xb[MT][4], s2[4], P[4][4];
+    load_x<MT, XP>((j < kGptqSegs ? xp : xq) + 64 * j, dx, xb);
+    if constexpr (FMT == EXQ_FMT_EXL2_QSCALE)
+      qfracs4(lds32(cp + j * kZeroRowBytes) >> csh, s2);
+    else
+      scales4(sp + j * kScaleRowBytes, s2);
+    exl2_unpack<B>(wrow + j * (B * kRowBytes), off, P);
+    scale_pairs<FMT>(P, s2, m2);
+    seg_mma<MT>(acc, P, xb);
+  }
+}
+
 // One EXL2 segment of width B, whole: its activations and scales, unpack,
 // scale, multiply. Each width of a mixed stage runs its own copy of all of
 // it, so that nothing after the width dispatch has to merge the per-width
@@ -844,6 +867,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (d.a & kDescUniform) {
         auto uni = [&](auto width) {
           constexpr int B = decltype(width)::value;
+          if (n == ((32 / B) < 16 ? 32 / B : 16)) {
+            run_full<FMT, B, MT, XP>(sl + lw, sl + ls, sl + lx, xbox, dx, t, m2, sl + lc, csh, acc);
+            return;
+          }
           run_uniform<FMT, B, MT, XP>(sl + lw, sl + ls, sl + lx, dx, t, n0, m2, sl + lc, csh, acc);
           if (n > kGptqSegs)
             run_uniform<FMT, B, MT, XP>(sl + lw + kGptqSegs * B * kRowBytes, sl + ls + kGptqSegs * kScaleRowBytes,

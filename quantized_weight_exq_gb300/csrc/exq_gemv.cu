@@ -264,16 +264,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // barrier is at stage j or past it and the parity wait is exact.
 __device__ __forceinline__ bool stage_wait(const uint32_t* seq, uint32_t j, uint32_t bar, uint32_t parity,
                                            volatile int* abort_flag, int limit) {
-  const bool leader = (threadIdx.x & 31) == 0;
   const volatile uint32_t* vseq = seq;
   for (int i = 0; i < limit; ++i) {
-    int state = 0;  // 1 = stage j landed, 2 = another role gave up
-    if (leader) state = (*vseq == j && mbar_try_wait_sleep(bar, parity)) ? 1 : (*abort_flag ? 2 : 0);
-    state = __shfl_sync(0xffffffffu, state, 0);
-    if (state == 1) return true;
-    if (state == 2) return false;
+    // every lane tests for itself (no broadcast from one lane); the warp goes
+    // on once all lanes saw the stage: a completed phase stays completed, so
+    // lanes that raced the completion agree in the next round
+    const bool ready = *vseq == j && mbar_try_wait_sleep(bar, parity);
+    if (__all_sync(0xffffffffu, ready)) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
   }
-  if (leader) {
+  if ((threadIdx.x & 31) == 0) {
     atomicOr(&g_gemv_err, kDevErrTimeout);
     *abort_flag = 1;
   }

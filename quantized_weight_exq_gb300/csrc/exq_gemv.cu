@@ -235,17 +235,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Bounded wait by lane 0 of a warp, result broadcast to the warp (all lanes
-// leave in the same round). A timeout is recorded and raises the abort flag;
-// a raised flag makes every other waiter give up too.
+// Bounded wait of a whole warp: every lane polls, and the warp leaves when a
+// vote says all lanes saw the phase complete (it stays complete until the
+// waiting warp itself acts on it) or one saw the abort flag, so all lanes
+// leave in the same round and no lane's result is broadcast from another.
+// A timeout is recorded and raises the abort flag; a raised flag makes every
+// other waiter give up too.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int limit) {
   const bool leader = (threadIdx.x & 31) == 0;
   for (int i = 0; i < limit; ++i) {
-    int state = 0;  // 1 = phase complete, 2 = another role gave up
-    if (leader) state = mbar_try_wait(bar, parity) ? 1 : (*abort_flag ? 2 : 0);
-    state = __shfl_sync(0xffffffffu, state, 0);
-    if (state == 1) return true;
-    if (state == 2) return false;
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
   }
   if (leader) {
     atomicOr(&g_gemv_err, kDevErrTimeout);
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kColGroups);  // the eight warps of the stage's set read it
+      mbar_init(smem_u32(&empty[i]), kColGroups * 32);  // every lane of the stage's set
       desc[i].seq = ~0u;                            // no stage yet
     }
     *abort_flag = 0;
@@ -923,8 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    mbar_arrive(smem_u32(&empty[slot]));  // each lane, once its reads of the slot are done
     slot += kSets;
     if (slot >= a.stages) {
       slot -= a.stages;

@@ -893,33 +893,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  d.whi, m2, sl + lc + kGptqSegs * kZeroRowBytes, csh, acc);
       }
     } else {
-      int rem = static_cast<int>(d.gpos);  // position of the stage's first segment in its group
-      const uint8_t* zr = sl + lc;         // zero word of the current group
-      const uint8_t* sr = sl + ls;         // scales of the current group
-      const uint8_t* wr = sl + lw + t * kRowBytes;
-      const uint8_t* xr = sl + lx;
-      uint32_t zlo[4], zhi[4], s2[4];
-      for (int j = 0; j < n; ++j) {
-        if (j == 0 || rem == 0) {  // this stage's first segment, or a new group
-          const uint32_t zw = lds32(zr) >> csh;
+      if (n == kGptqSegs && a.gs_seg == 4 && d.gpos == 0) {
+        // a whole stage of two 128-row groups: every address is a
+        // compile-time offset and the group change needs no test
+#pragma unroll
+        for (int j = 0; j < kGptqSegs; ++j) {
+          uint32_t zlo[4], zhi[4], s2[4];
+          const uint32_t zw = lds32(sl + lc + (j / 4) * kZeroRowBytes) >> csh;
 #pragma unroll
           for (int c = 0; c < 4; ++c) gptq_zero_consts((zw >> (4 * c)) & 0xFu, zlo[c], zhi[c]);
-          scales4(sr, s2);
-        }
-        uint32_t xb[MT][4];
-        load_x<MT, XP>(xr, dx, xb);
-        const uint4 wq = lds128(wr);
-        uint32_t P[4][4];
+          scales4(sl + ls + (j / 4) * kScaleRowBytes, s2);
+          uint32_t xb[MT][4];
+          load_x<MT, XP>(sl + lx + 64 * j, dx, xb);
+          const uint4 wq = lds128(sl + lw + t * kRowBytes + j * 4 * kRowBytes);
+          uint32_t P[4][4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) unpack8_gptq(comp(wq, c), zlo[c], zhi[c], P[c]);
-        scale_pairs<FMT>(P, s2, s2);
-        seg_mma<MT>(acc, P, xb);
-        wr += 4 * kRowBytes;
-        xr += 64;
-        if (++rem == a.gs_seg) {
-          rem = 0;
-          zr += kZeroRowBytes;
-          sr += kScaleRowBytes;
+          for (int c = 0; c < 4; ++c) unpack8_gptq(comp(wq, c), zlo[c], zhi[c], P[c]);
+          scale_pairs<FMT>(P, s2, s2);
+          seg_mma<MT>(acc, P, xb);
+        }
+      } else {
+        int rem = static_cast<int>(d.gpos);  // position of the stage's first segment in its group
+        const uint8_t* zr = sl + lc;         // zero word of the current group
+        const uint8_t* sr = sl + ls;         // scales of the current group
+        const uint8_t* wr = sl + lw + t * kRowBytes;
+        const uint8_t* xr = sl + lx;
+        uint32_t zlo[4], zhi[4], s2[4];
+        for (int j = 0; j < n; ++j) {
+          if (j == 0 || rem == 0) {  // this stage's first segment, or a new group
+            const uint32_t zw = lds32(zr) >> csh;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) gptq_zero_consts((zw >> (4 * c)) & 0xFu, zlo[c], zhi[c]);
+            scales4(sr, s2);
+          }
+          uint32_t xb[MT][4];
+          load_x<MT, XP>(xr, dx, xb);
+          const uint4 wq = lds128(wr);
+          uint32_t P[4][4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) unpack8_gptq(comp(wq, c), zlo[c], zhi[c], P[c]);
+          scale_pairs<FMT>(P, s2, s2);
+          seg_mma<MT>(acc, P, xb);
+          wr += 4 * kRowBytes;
+          xr += 64;
+          if (++rem == a.gs_seg) {
+            rem = 0;
+            zr += kZeroRowBytes;
+            sr += kScaleRowBytes;
+          }
         }
       }
     }

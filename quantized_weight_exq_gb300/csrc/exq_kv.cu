@@ -27,6 +27,23 @@ namespace {
 
 constexpr int kWarps = 8;  // groups per 256-thread block
 
+// x / C rounded to nearest even in fp32, for x an fp16 magnitude (amax) and
+// C = qmax in {7, 31, 127}: the quotient x y with y = RN(1 / C), corrected by
+// one fma with its remainder (the division-by-a-constant method of Cornea,
+// Harrison and Tang, "Scientific Computing on Itanium-based Systems", FMA
+// correction step). For these C every positive finite fp16 x gives the
+// correctly rounded quotient, checked exhaustively against exact rational
+// rounding in tests/test_kv_division.py; three instructions instead of a
+// full IEEE division.
+template <int C>
+__device__ __forceinline__ float div_by_const(float x) {
+  // RN(1 / C), written out so that it does not depend on constant folding
+  constexpr float y = C == 7 ? 0x1.24924ap-3f : C == 31 ? 0x1.084210p-5f : 0x1.020408p-7f;
+  const float q = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q, static_cast<float>(C), x);
+  return __fmaf_rn(r, y, q);
+}
+
 template <int VPL>  // values per lane: D / 32
 struct Vec;
 template <>
@@ -135,7 +152,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     // non-negative floats order as their bit patterns
     amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
-    const __half s16 = __float2half_rn(__fdiv_rn(amax, static_cast<float>(kQmax)));
+    static_assert(kQmax == 7 || kQmax == 31 || kQmax == 127, "div_by_const is checked for these only");
+    const __half s16 = __float2half_rn(div_by_const<kQmax>(amax));
     const float s = __half2float(s16);
     const float inv = s != 0.f ? __frcp_rn(s) : 0.f;
 

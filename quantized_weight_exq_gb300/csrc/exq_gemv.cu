@@ -12,10 +12,13 @@
 // GB300 mapping:
 //  * Work is the list of (248-column tile, 32-row segment) units, tile-major,
 //    over all layers of the launch (their tiles numbered one after another).
-//    Every CTA (one per SM) takes an equal contiguous share, so all SMs
-//    stream the same number of bytes whatever N and K are. A share falls into
-//    pieces, one per tile it touches.
-//  * Warp 16 is the producer. It cuts each piece into stages of at most 32
+//    Every CTA takes an equal contiguous share, so all SMs stream the same
+//    number of bytes whatever N and K are. A share falls into pieces, one per
+//    tile it touches. For M <= 8 a CTA has one consumer set (8 warps) and
+//    two CTAs share an SM (a ring of two slots each), so that on each SM a
+//    CTA of the next call can start while the other CTA still finishes this
+//    one; for M <= 16 a CTA has two sets and owns its SM.
+//  * The warp after the consumers is the producer. It cuts each piece into stages of at most 32
 //    packed word rows (EXL2: the longest run of whole segments that fits, at
 //    most 16, one compare per lane on the segment table's prefix sums; GPTQ:
 //    8-segment blocks aligned to 256 rows) and moves a stage
@@ -25,7 +28,8 @@
 //    4-byte asynchronous copies. All of it completes on the slot's "full"
 //    mbarrier. The weight copies of the first slots are issued before the
 //    wait on the previous kernel (they are model state); x after it.
-//  * Warps 0-15 consume, in two sets of eight: stage i goes to set i % 2, and
+//  * The consumer warps form one or two sets of eight: stage i goes to set
+//    i % sets, and
 //    warp w of the set owns columns 32 w .. 32 w + 31 of the tile for every
 //    segment of the stage, so the fixed cost of a stage (wait, descriptor,
 //    release) is paid once per up to 16 segments. Lane (g = lane / 4,
@@ -82,9 +86,12 @@ __device__ unsigned g_gemv_err;
 constexpr int kTN = 248;                 // columns per tile (992-byte rows: see above)
 constexpr int kTP = 256;                 // columns per tile in the partial sums (8 warps x 32)
 constexpr int kColGroups = 8;            // 32 columns each
-constexpr int kSets = 2;                 // consumer sets: stage i is read by set i % 2
-constexpr int kConsumerWarps = kSets * kColGroups;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Consumer sets: stage i is read by set i % sets. The kernels for M <= 8
+// (one 8-token block) have one set per CTA and run two CTAs per SM where a
+// ring of two slots fits half an SM's shared memory, so that one CTA can
+// start its next call while the other still finishes; those for M <= 16 have
+// two sets in one CTA per SM.
+__host__ __device__ constexpr int sets_of(int MT) { return MT == 1 ? 1 : 2; }
 constexpr int kMaxSegs = 16;             // EXL2 segments per stage
 constexpr int kGptqSegs = 8;             // GPTQ segments per stage (256 rows of K); segments per x box
 constexpr int kRowsPerStage = 32;        // packed word rows per stage (box height)
@@ -625,8 +632,9 @@ __device__ __forceinline__ const uint8_t* run_mixed(const uint8_t* row, const ui
 // MT: 8-token blocks (1 for M <= 8, 2 for M <= 16).
 
 template <int FMT, int MT, bool XP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_of(MT))
     gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
+  constexpr int sets = sets_of(MT);
   extern __shared__ uint8_t smem_raw[];
   // aligned by pointer arithmetic on the shared array, so that every access
   // through it stays a shared-memory access
@@ -654,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = static_cast<int>(gridDim.x);
   const int u0 = share_begin(blockIdx.x, a.total, G), u1 = share_begin(blockIdx.x + 1, a.total, G);
 
-  if (warp == kConsumerWarps) {
+  if (warp == sets * kColGroups) {
     // ------------------------------------------------------------ producer
     if (a.starve) return;  // test hook: nothing is issued, nothing is in flight
     // the layers this CTA's share touches
@@ -827,11 +835,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         seg += n;
       }
       // the other set closes the piece too
-      if (ok) ok = mark(kDescLast, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16));
+      if (sets == 2 && ok) ok = mark(kDescLast, static_cast<uint32_t>(tile) | (static_cast<uint32_t>(layer) << 16));
     }
     if (!waited) release_x();
     // one end mark per set
-    const bool ended = ok && mark(kDescEnd, 0u) && mark(kDescEnd, 0u);
+    const bool ended = ok && mark(kDescEnd, 0u) && (sets == 1 || mark(kDescEnd, 0u));
     // after a give-up no consumer will wait for the copies still in flight:
     // they land before the CTA may exit (otherwise the consumers saw them all)
     if (!ended && lane == 0)
@@ -860,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Acc<MT> acc;
   zero_acc<MT>(acc);
   int slot = set, fphase = 0;  // this set's first stage (stages >= 2)
-  for (uint32_t j = static_cast<uint32_t>(set);; j += kSets) {
+  for (uint32_t j = static_cast<uint32_t>(set);; j += sets) {
     if (!stage_wait(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag, a.sleep_limit)) break;
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
@@ -952,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     mbar_arrive(smem_u32(&empty[slot]));  // each lane, once its reads of the slot are done
-    slot += kSets;
+    slot += sets;
     if (slot >= a.stages) {
       slot -= a.stages;
       fphase ^= 1;
@@ -964,8 +972,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arrivals at the column group's counter adds them in order.
       const int tile = static_cast<int>(d.c & 0xFFFFu);
       const int first = share_owner(tile * a.S, a.total, G);
-      const int P2 = kSets * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
-      const int pslot = kSets * (static_cast<int>(blockIdx.x) - first) + set;
+      const int P2 = sets * (share_owner(tile * a.S + a.S - 1, a.total, G) - first + 1);
+      const int pslot = sets * (static_cast<int>(blockIdx.x) - first) + set;
       float* part = a.partials + (static_cast<size_t>(tile) * a.max_pieces + pslot) * a.M * kTP;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
@@ -1046,9 +1054,12 @@ int variant_index(int fmt, int M, bool xp) { return 4 * (fmt - 1) + 2 * (xp ? 1 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kSmemPerCta = 227 * 1024;  // one CTA per SM (the sm_103 per-block maximum)
+constexpr int kSmemHalf = 113 * 1024;    // two CTAs per SM (each also takes 1 KB the system reserves)
 
 struct Plan {
   int G, S, n_tiles, total, max_pieces, stages, slot_bytes, off_bar;
+  int sets;                   // consumer sets per CTA: sets_of(MT) of the kernel for M
+  int per_sm;                 // CTAs per SM: 2 when two one-set CTAs fit an SM
   int tile0[kMaxLayers + 1];  // first global tile of each layer; tile0[n] = n_tiles
   bool gather;                // some layer has a permutation: x is gathered per layer
   size_t smem;                // dynamic shared memory bytes (with the alignment slack)
@@ -1074,24 +1085,30 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
   const long long total = static_cast<long long>(p.n_tiles) * p.S;
   if (total >= (1ll << 31)) return false;
   p.total = static_cast<int>(total);
-  int G = sm_count;
+  p.slot_bytes = slot_bytes_for(M);
+  const size_t table = w[0].format != EXQ_FMT_GPTQ4 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
+  const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment tables, alignment slack
+  // one set per CTA and two CTAs per SM where a ring of two slots fits half
+  // the shared memory (M <= 8): a CTA of the next call can then start on an
+  // SM while the other CTA there still works on this one
+  p.sets = sets_of(M <= 8 ? 1 : 2);
+  p.per_sm = p.sets == 1 && 2 * static_cast<size_t>(p.slot_bytes) + fixed <= static_cast<size_t>(kSmemHalf) ? 2 : 1;
+  const long long budget = p.per_sm == 2 ? kSmemHalf : kSmemPerCta;
+  int G = p.per_sm * sm_count;
   if (const char* env = std::getenv("EXQ_GEMV_CTAS")) {  // CTA-count override for tests of the split
     const int v = std::atoi(env);
     if (v > 0) G = v;
   }
   p.G = std::max(1, std::min(G, p.total));
-  p.slot_bytes = slot_bytes_for(M);
-  const size_t table = w[0].format != EXQ_FMT_GPTQ4 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
-  const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment tables, alignment slack
-  const long long room = static_cast<long long>(kSmemPerCta) - static_cast<long long>(fixed);
+  const long long room = budget - static_cast<long long>(fixed);
   p.stages = static_cast<int>(std::min<long long>(kMaxStages, room / p.slot_bytes));
   if (p.stages < 2) return false;
   p.off_bar = p.stages * p.slot_bytes;
   p.smem = static_cast<size_t>(p.off_bar) + fixed;
   // a tile of S units meets at most (S - 1) / s + 2 shares of at least s
-  // units; each leaves one partial per K group
+  // units; each leaves one partial per consumer set
   const int min_share = std::max(1, p.total / p.G);
-  p.max_pieces = 2 * std::min(p.G, (p.S - 1) / min_share + 2);
+  p.max_pieces = p.sets * std::min(p.G, (p.S - 1) / min_share + 2);
   p.ws_partials = align_up(static_cast<size_t>(p.n_tiles) * p.max_pieces * M * kTP * 4, 256);
   p.ws_bytes = kCounterBytes + p.ws_partials +
                (p.gather ? align_up(static_cast<size_t>(n) * M * w[0].K * 2, 256) : 0);
@@ -1129,7 +1146,8 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
     std::lock_guard<std::mutex> lock(g_attr_mutex);
     bool& done = g_attr_done[dev][variant_index(w0.format, M, plan.gather)];
     if (!done) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess ||
+          cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return EXQ_ERR_CUDA;
       done = true;
     }
@@ -1219,7 +1237,7 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(plan.G, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3((plan.sets * kColGroups + 1) * 32, 1, 1);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
   cfg.attrs = attrs;

@@ -107,10 +107,10 @@ constexpr int kMaxStages = 6;
 constexpr int kPreWaitStages = 3;
 // try_wait rounds before giving up. The producer polls (a round without a
 // suspend hint returns after a short, hardware-chosen time): it must issue
-// the next copy as soon as a slot frees. Consumers sleep in the wait, up to
-// kWaitHintNs a round, so that a set waiting for data does not take issue
-// slots from the set that is computing (1.2 % faster on the 70B stream than
-// polling consumers).
+// the next copy as soon as a slot frees. Consumers of a two-set CTA sleep in
+// the wait, up to kWaitHintNs a round, so that a set waiting for data does
+// not take issue slots from the set that is computing (1.2 % faster on the
+// 70B stream than polling there); those of a one-set CTA poll.
 constexpr int kWaitLimit = 1 << 24;
 constexpr int kSleepLimit = 1 << 17;       // consumer rounds: at most 2.6 s
 constexpr uint32_t kWaitHintNs = 20000;
@@ -276,6 +276,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // stage j's descriptor, with seq = j, only after the slot's previous stage
 // was released, hence after it landed; once the descriptor shows j, the
 // barrier is at stage j or past it and the parity wait is exact.
+// SLEEP: the waiting warps suspend in try_wait (two sets per CTA: a set that
+// waits then leaves the issue slots to the one that computes); otherwise
+// they poll (one set per CTA: 0.5 % faster on the 70B stream than sleeping).
+template <bool SLEEP>
 __device__ __forceinline__ bool stage_wait(const uint32_t* seq, uint32_t j, uint32_t bar, uint32_t parity,
                                            volatile int* abort_flag, int limit) {
   const volatile uint32_t* vseq = seq;
@@ -283,7 +287,7 @@ __device__ __forceinline__ bool stage_wait(const uint32_t* seq, uint32_t j, uint
     // every lane tests for itself (no broadcast from one lane); the warp goes
     // on once all lanes saw the stage: a completed phase stays completed, so
     // lanes that raced the completion agree in the next round
-    const bool ready = *vseq == j && mbar_try_wait_sleep(bar, parity);
+    const bool ready = *vseq == j && (SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity));
     if (__all_sync(0xffffffffu, ready)) return true;
     if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
   }
@@ -869,7 +873,9 @@ __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_
   zero_acc<MT>(acc);
   int slot = set, fphase = 0;  // this set's first stage (stages >= 2)
   for (uint32_t j = static_cast<uint32_t>(set);; j += sets) {
-    if (!stage_wait(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag, a.sleep_limit)) break;
+    if (!stage_wait<(sets > 1)>(&desc[slot].seq, j, smem_u32(&full[slot]), fphase, abort_flag,
+                                sets > 1 ? a.sleep_limit : a.wait_limit))
+      break;
     const Desc d = desc[slot];
     if (d.a & kDescEnd) break;
     const uint8_t* sl = smem + slot * a.slot_bytes;

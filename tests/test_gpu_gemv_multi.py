@@ -195,3 +195,18 @@ def test_decode_stream_70b_groups_sampled(env, names):
     ys = _multi(exq, torch, [w for w, _, _ in layers], x)
     for n, y, (_, cols, W_ref) in zip(names, ys, layers):
         check_matmul(y[:, cols], O.matmul(x, W_ref), f"70b group {names} layer {n}")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_gemv_multi_four_long_layers(env, M):
+    exq, torch = env
+    # four EXL2 layers with K = 28672 (the down projection's K): at M = 8 their
+    # segment tables and a two-slot ring no longer fit half an SM, so the
+    # one-set kernel runs one CTA per SM with a five-slot ring; at M = 1 two
+    # CTAs share an SM. Both against the oracle.
+    K = 28672
+    ws, Ws = _exl2_group(exq, K, (128, 248, 64, 200), (True, True, False, True), seed=90 + M)
+    x = synth.activations(M, K, seed=M + 90)
+    ys = _multi(exq, torch, ws, x)
+    for i, (y, W) in enumerate(zip(ys, Ws)):
+        check_matmul(y, O.matmul(x, W), f"four long layers, layer {i}, M={M}")

@@ -181,8 +181,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Bounded wait of a whole warp. VOTE: every lane tests, and the warp leaves
 // when a vote says all saw the phase complete (it stays complete until this
 // warp acts on it) or one saw the abort flag; otherwise lane 0 tests and
-// broadcasts. The vote made the EXL2 dequantisers 9-18 % faster and GPTQ's
-// 0.8 % slower, so each format keeps the faster one.
+// broadcasts. With the vote (and the dequantisers' per-lane release) the
+// EXL2 formats ran 9-18 % faster; for GPTQ the vote alone made the large
+// shapes 1-2 % slower, so GPTQ keeps the lane-0 test.
 template <bool VOTE>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                int limit) {
@@ -332,7 +333,7 @@ __device__ __forceinline__ void exl2_segment(const uint32_t* rows, int col, uint
 template <int FMT, bool XP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs a) {
-  constexpr bool kVote = FMT != EXQ_FMT_GPTQ4;  // the dequantisers' wait and arrive style (see mbar_wait_warp)
+  constexpr bool kVote = FMT != EXQ_FMT_GPTQ4;  // the dequantisers' wait style (see mbar_wait_warp)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* bar_area = smem + kStages * kStageBytes;
@@ -360,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      // EXL2: every lane of the dequantisers arrives; GPTQ: one per warp
-      mbar_init(smem_u32(&aready[s]), FMT == EXQ_FMT_GPTQ4 ? kDequantWarps : kDequantWarps * 32);
+      mbar_init(smem_u32(&aready[s]), kDequantWarps * 32);  // every lane of the dequantisers
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(accum), 1);
@@ -521,12 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(tmem + lane_base + kTmemA + s * kAStageCols + h * 16, r);
       tmem_st_wait();
       tc_fence_before();
-      if constexpr (kVote) {
-        mbar_arrive(smem_u32(&aready[s]));  // each lane, its stores done
-      } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&aready[s]));
-      }
+      mbar_arrive(smem_u32(&aready[s]));  // each lane, its stores done
     }
 
     // ------------------------------------------------------------ epilogue

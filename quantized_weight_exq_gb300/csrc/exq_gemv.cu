@@ -29,9 +29,8 @@
 //    mbarrier. The weight copies of the first slots are issued before the
 //    wait on the previous kernel (they are model state); x after it.
 //  * The consumer warps form one or two sets of eight: stage i goes to set
-//    i % sets, and
-//    warp w of the set owns columns 32 w .. 32 w + 31 of the tile for every
-//    segment of the stage, so the fixed cost of a stage (wait, descriptor,
+//    i % sets, and warp w of the set owns columns 32 w .. 32 w + 31 of the
+//    tile for every segment of the stage, so the fixed cost of a stage (wait, descriptor,
 //    release) is paid once per up to 16 segments. Lane (g = lane / 4,
 //    t = lane % 4) owns the four columns 4g .. 4g+3 (one 16-byte read per
 //    word row: eight lanes read a whole line) and the 8-code block t of every
@@ -45,9 +44,9 @@
 //    fp32 accumulate) as the A operand of a swapped product (A = W^T,
 //    B = x^T), into four independent accumulators. A stage whose EXL2
 //    segments share one width runs a loop compiled for that width.
-//  * A piece's last stage carries a flush mark; right after it the producer
-//    queues an empty stage with the mark for the other set, so both sets
-//    close every piece. On the mark each warp writes fp32 partial sums of its
+//  * A piece's last stage carries a flush mark; with two sets the producer
+//    queues an empty stage with the mark for the other set right after it,
+//    so both sets close every piece. On the mark each warp writes fp32 partial sums of its
 //    32 columns to the caller's workspace; the warp that arrives last at its
 //    (tile, column group) counter adds the tile's partials in piece order,
 //    writes y and puts the counter back to zero. Deterministic, and no warp
@@ -268,9 +267,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
-// The wait of a consumer set for stage j of its slot. Both sets use every
-// slot in turn, so a set's successive stages in one slot are two phases of
-// its full barrier apart, and a parity wait alone also passes while the
+// The wait of a consumer set for stage j of its slot. With two sets both use
+// every slot in turn, so with an odd slot count a set's successive stages in
+// one slot are two phases of its full barrier apart, and a parity wait alone also passes while the
 // barrier is still short of the other set's stage in between (same parity
 // two phases back). The descriptor closes that gap: the producer writes
 // stage j's descriptor, with seq = j, only after the slot's previous stage

@@ -41,7 +41,7 @@ EncodeTiled tensor_map_encoder() {
 }
 
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapL2promotion promotion) {
   EncodeTiled enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t gdim[2] = {inner, outer};
@@ -49,7 +49,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uin
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
   return enc(map, type, 2, const_cast<void*>(base), gdim, gstride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_SWIZZLE_NONE, promotion,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -1201,12 +1201,18 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
       l.tile0 = INT_MAX;
       continue;
     }
+    // A tile's 992-byte word row starts on a 32-byte boundary, rarely on a
+    // 256-byte one: with 256-byte L2 promotion each row pulled about 1216
+    // bytes, and the edges again for the neighbouring tile (another CTA,
+    // another time). 64-byte promotion cut the DRAM reads of a 70B gate+up
+    // call from 1.146 to 1.091 times the packed bytes.
     if (!encode_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[i].qweight, w[i].N, w[i].n_word_rows,
-                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage))
+                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage, CU_TENSOR_MAP_L2_PROMOTION_L2_64B))
       return EXQ_ERR_CUDA;
     // fp16 scale rows (two-level scales come without a tensor map)
     if (w[i].scales && !encode_2d(&maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, w[i].scales, w[i].N, scale_rows,
-                                  static_cast<uint64_t>(w[i].N) * 2, kTN, kScaleRows))
+                                  static_cast<uint64_t>(w[i].N) * 2, kTN, kScaleRows,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_64B))
       return EXQ_ERR_CUDA;
     l.seg_off = w[i].seg_word_off;
     l.qzeros = w[i].qzeros;

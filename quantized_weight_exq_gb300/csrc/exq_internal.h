@@ -37,9 +37,11 @@ EncodeTiled tensor_map_encoder();
 
 // A 2-D tiled tensor map without swizzle: dims {inner, outer} elements, the
 // outer stride in bytes, box {box_inner, box_outer}; elements outside the
-// tensor read as zero. False if the driver rejects it.
+// tensor read as zero; `promotion` sets how much L2 fetches around each
+// access. False if the driver rejects it.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+               uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapL2promotion promotion = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 // n layers (1..EXQ_GEMV_MAX_LAYERS) of one format and K that share x
 exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uint16_t* const* y, void* workspace,

@@ -18,12 +18,12 @@
 //    two CTAs share an SM (a ring of two slots each), so that on each SM a
 //    CTA of the next call can start while the other CTA still finishes this
 //    one; for M <= 16 a CTA has two sets and owns its SM.
-//  * The warp after the consumers is the producer. It cuts each piece into stages of at most 32
-//    packed word rows (EXL2: the longest run of whole segments that fits, at
-//    most 16, one compare per lane on the segment table's prefix sums; GPTQ:
-//    8-segment blocks aligned to 256 rows) and moves a stage
-//    with tensor-map copies into one slot of a shared-memory ring: the word
-//    rows (a 32-row x 248-column box), the scale rows (a 16 x 248 box) and the
+//  * The warp after the consumers is the producer. It cuts each piece into
+//    stages of at most 32 packed word rows, 40 for EXL2 at small M (EXL2: the
+//    longest run of whole segments that fits, at most 16, one compare per
+//    lane on the segment table's prefix sums; GPTQ: 8-segment blocks aligned
+//    to 256 rows) and moves a stage with tensor-map copies into one slot of a
+//    shared-memory ring: the word rows (a 32- or 40-row x 248-column box), the scale rows (a 16 x 248 box) and the
 //    stage's activations (one or two 256 x M boxes); GPTQ zero rows follow as
 //    4-byte asynchronous copies. All of it completes on the slot's "full"
 //    mbarrier. The weight copies of the first slots are issued before the
@@ -93,7 +93,16 @@ constexpr int kColGroups = 8;            // 32 columns each
 __host__ __device__ constexpr int sets_of(int MT) { return MT == 1 ? 1 : 2; }
 constexpr int kMaxSegs = 16;             // EXL2 segments per stage
 constexpr int kGptqSegs = 8;             // GPTQ segments per stage (256 rows of K); segments per x box
-constexpr int kRowsPerStage = 32;        // packed word rows per stage (box height)
+// Packed word rows per stage (the weight box's height), a kernel parameter
+// ROWS: 32 in general (GPTQ: 8 segments of 4 rows), 40 for EXL2 where two
+// slots of that height and the segment tables still fit half an SM (M <= 4
+// on the 70B shapes): the stage's fixed cost is then spread over a quarter
+// more segments (1.1 % faster on the 70B stream). Every call that fits takes
+// 40, small ones too: a stream that switched between 32-row launches (small
+// shares) and 40-row ones was 1.8 % slower than either, since consecutive
+// launches then ask for different shared-memory sizes.
+constexpr int kRowsShort = 32;
+constexpr int kRowsLong = 40;
 constexpr int kScaleRows = 16;           // scale (and GPTQ zero) rows per stage
 constexpr int kCounterBytes = 64 * 1024; // workspace counter region (zero between calls)
 constexpr int kMaxStages = 6;
@@ -114,23 +123,27 @@ constexpr int kWaitLimit = 1 << 24;
 constexpr int kSleepLimit = 1 << 17;       // consumer rounds: at most 2.6 s
 constexpr uint32_t kWaitHintNs = 20000;
 
-// slot layout (bytes): word rows | scale rows | GPTQ zero rows | x [2][M][256]
+// slot layout (bytes): word rows [ROWS] | scale rows | GPTQ zero rows | x [2][M][256]
 constexpr int kRowBytes = kTN * 4;                         // 992
 constexpr int kScaleRowBytes = kTN * 2;                    // 496
-constexpr int kSlotW = 0;
-constexpr int kSlotS = kSlotW + kRowsPerStage * kRowBytes;
-constexpr int kSlotZ = ((kSlotS + kScaleRows * kScaleRowBytes + 127) / 128) * 128;
 constexpr int kZeroRowBytes = 128;                         // 31 zero words of a tile, one row per group
-constexpr int kSlotX = kSlotZ + kScaleRows * kZeroRowBytes;
 constexpr int kXBox = 256;                                 // activations per x box (8 segments)
 constexpr int kXBoxBytes = kXBox * 2;                      // per token
-static_assert(kSlotS % 128 == 0 && kSlotZ % 128 == 0 && kSlotX % 128 == 0,
+constexpr int kSlotW = 0;
+__host__ __device__ constexpr int slot_s(int rows) { return kSlotW + rows * kRowBytes; }
+__host__ __device__ constexpr int slot_z(int rows) {
+  return ((slot_s(rows) + kScaleRows * kScaleRowBytes + 127) / 128) * 128;
+}
+__host__ __device__ constexpr int slot_x(int rows) { return slot_z(rows) + kScaleRows * kZeroRowBytes; }
+static_assert(slot_s(kRowsShort) % 128 == 0 && slot_z(kRowsShort) % 128 == 0 && slot_x(kRowsShort) % 128 == 0 &&
+                  slot_s(kRowsLong) % 128 == 0 && slot_z(kRowsLong) % 128 == 0 && slot_x(kRowsLong) % 128 == 0,
               "tensor-map destinations start on 128-byte boundaries");
 static_assert(kTN % 8 == 0 && kTN / 8 <= 32, "a tile's zero words fit one warp");
 static_assert(kMaxSegs <= 2 * kGptqSegs, "a stage's activations fit two x boxes");
+static_assert(kGptqSegs * 4 == kRowsShort, "a GPTQ stage fills the short box");
 
-__host__ __device__ constexpr int slot_bytes_for(int M) {
-  return ((kSlotX + 2 * M * kXBoxBytes + 1023) / 1024) * 1024;
+__host__ __device__ constexpr int slot_bytes_for(int M, int rows) {
+  return ((slot_x(rows) + 2 * M * kXBoxBytes + 1023) / 1024) * 1024;
 }
 
 constexpr int kMaxLayers = EXQ_GEMV_MAX_LAYERS;  // layers of one launch (they share x and K)
@@ -566,12 +579,12 @@ __device__ __forceinline__ void run_uniform(const uint8_t* wp, const uint8_t* sp
   }
 }
 
-// EXL2, a whole stage of width B (32 / B segments, at most 16): the loop
+// EXL2, a whole stage of width B (ROWS / B segments, at most 16): the loop
 // runs a compile-time count, so every address is an immediate offset
-template <int FMT, int B, int MT, bool XP>
+template <int FMT, int B, int MT, bool XP, int ROWS>
 __device__ __forceinline__ void run_full(const uint8_t* wp, const uint8_t* sp, const uint8_t* xp, int xbox, int dx,
                                          int t, const uint32_t (&m2)[4], const uint8_t* cp, int csh, Acc<MT>& acc) {
-  constexpr int kN = (32 / B) < 16 ? 32 / B : 16;
+  constexpr int kN = (ROWS / B) < 16 ? ROWS / B : 16;
   const uint8_t* wrow = wp + blk_row_bytes<B>(t);
   const uint32_t off = blk_bit<B>(t);
   const uint8_t* xq = xp + xbox - 64 * kGptqSegs;  // segments 8.. read the second x box
@@ -634,10 +647,11 @@ __device__ __forceinline__ const uint8_t* run_mixed(const uint8_t* row, const ui
 // ---------------------------------------------------------------- the kernel
 // MT: 8-token blocks (1 for M <= 8, 2 for M <= 16).
 
-template <int FMT, int MT, bool XP>
+template <int FMT, int MT, bool XP, int ROWS>
 __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_of(MT))
     gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
   constexpr int sets = sets_of(MT);
+  constexpr int kSlotS = slot_s(ROWS), kSlotZ = slot_z(ROWS), kSlotX = slot_x(ROWS);
   extern __shared__ uint8_t smem_raw[];
   // aligned by pointer arithmetic on the shared array, so that every access
   // through it stays a shared-memory access
@@ -691,7 +705,7 @@ __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_
     }
     const uint32_t x_bytes = static_cast<uint32_t>(a.M) * kXBoxBytes;  // one x box
     // two-level scales arrive by cp.async, not in the transaction count
-    const uint32_t tx_w = kRowsPerStage * kTN * 4 + (FMT == EXQ_FMT_EXL2_QSCALE ? 0 : kScaleRows * kTN * 2);
+    const uint32_t tx_w = ROWS * kTN * 4 + (FMT == EXQ_FMT_EXL2_QSCALE ? 0 : kScaleRows * kTN * 2);
     int slot = 0, ephase = 0, issued = 0, npend = 0;
     // the piece's layer: its index, tensor maps, first row of x, GPTQ zeros
     const CUtensorMap* mw = &maps.w[0];
@@ -803,7 +817,7 @@ __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_
           zrows = (seg + n - 1) / a.gs_seg - srow + 1;
         } else {
           // the longest run of valid segments from seg (at most sixteen) whose
-          // widths add up to at most 32 rows, straight from the word-row prefix
+          // widths add up to at most ROWS rows, straight from the word-row prefix
           // sums: lane j tests segment seg + j
           const int sk = seg + lane;
           const bool cand = lane < kMaxSegs && sk < sb;
@@ -812,7 +826,7 @@ __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_
           const uint32_t e0 = cand ? ltbl[sk] : 0u, e1 = cand ? ltbl[sk + 1] : 0u;
           const int b = static_cast<int>(e1) - static_cast<int>(e0);
           const bool good = cand && valid_width(b) && e1 <= static_cast<uint32_t>(ly.n_word_rows) &&
-                            static_cast<int>(e1 - base) <= kRowsPerStage;
+                            static_cast<int>(e1 - base) <= ROWS;
           const unsigned stop = __ballot_sync(0xffffffffu, !good);
           n = __ffs(stop) - 1;  // leading lanes that fit (stop always has a bit at or below lane 16)
           wlo = __reduce_or_sync(0xffffffffu, lane < n && lane < 8 ? static_cast<uint32_t>(b) << (4 * lane) : 0u);
@@ -887,8 +901,8 @@ __global__ void __launch_bounds__((sets_of(MT) * kColGroups + 1) * 32, 3 - sets_
       if (d.a & kDescUniform) {
         auto uni = [&](auto width) {
           constexpr int B = decltype(width)::value;
-          if (n == ((32 / B) < 16 ? 32 / B : 16)) {
-            run_full<FMT, B, MT, XP>(sl + lw, sl + ls, sl + lx, xbox, dx, t, m2, sl + lc, csh, acc);
+          if (n == ((ROWS / B) < 16 ? ROWS / B : 16)) {
+            run_full<FMT, B, MT, XP, ROWS>(sl + lw, sl + ls, sl + lx, xbox, dx, t, m2, sl + lc, csh, acc);
             return;
           }
           run_uniform<FMT, B, MT, XP>(sl + lw, sl + ls, sl + lx, dx, t, n0, m2, sl + lc, csh, acc);
@@ -1039,22 +1053,31 @@ namespace {
 
 using KernelFn = void (*)(GemvMaps, GemvArgs);
 
+// long: 40-row stages (EXL2 formats, M <= 8 kernels only)
 template <int FMT, bool XP>
-KernelFn pick_for(int M) {
-  return M <= 8 ? gemv_kernel<FMT, 1, XP> : gemv_kernel<FMT, 2, XP>;
+KernelFn pick_for(int M, bool long_rows) {
+  if constexpr (FMT == EXQ_FMT_GPTQ4)
+    return M <= 8 ? gemv_kernel<FMT, 1, XP, kRowsShort> : gemv_kernel<FMT, 2, XP, kRowsShort>;
+  else
+    return M > 8 ? gemv_kernel<FMT, 2, XP, kRowsShort>
+           : long_rows ? gemv_kernel<FMT, 1, XP, kRowsLong> : gemv_kernel<FMT, 1, XP, kRowsShort>;
 }
 
 // XP: x comes from the gather kernel, pair-interleaved
 template <bool XP>
-KernelFn pick_fmt(int fmt, int M) {
-  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4, XP>(M)
-         : fmt == EXQ_FMT_EXL2 ? pick_for<EXQ_FMT_EXL2, XP>(M)
-                               : pick_for<EXQ_FMT_EXL2_QSCALE, XP>(M);
+KernelFn pick_fmt(int fmt, int M, bool long_rows) {
+  return fmt == EXQ_FMT_GPTQ4 ? pick_for<EXQ_FMT_GPTQ4, XP>(M, long_rows)
+         : fmt == EXQ_FMT_EXL2 ? pick_for<EXQ_FMT_EXL2, XP>(M, long_rows)
+                               : pick_for<EXQ_FMT_EXL2_QSCALE, XP>(M, long_rows);
 }
 
-KernelFn pick_kernel(int fmt, int M, bool xp) { return xp ? pick_fmt<true>(fmt, M) : pick_fmt<false>(fmt, M); }
+KernelFn pick_kernel(int fmt, int M, bool xp, bool long_rows) {
+  return xp ? pick_fmt<true>(fmt, M, long_rows) : pick_fmt<false>(fmt, M, long_rows);
+}
 
-int variant_index(int fmt, int M, bool xp) { return 4 * (fmt - 1) + 2 * (xp ? 1 : 0) + (M <= 8 ? 0 : 1); }
+int variant_index(int fmt, int M, bool xp, bool long_rows) {
+  return 8 * (fmt - 1) + 4 * (xp ? 1 : 0) + 2 * (long_rows ? 1 : 0) + (M <= 8 ? 0 : 1);
+}
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -1063,6 +1086,7 @@ constexpr int kSmemHalf = 113 * 1024;    // two CTAs per SM (each also takes 1 K
 
 struct Plan {
   int G, S, n_tiles, total, max_pieces, stages, slot_bytes, off_bar;
+  int rows;                   // word rows per stage (kRowsShort or kRowsLong)
   int sets;                   // consumer sets per CTA: sets_of(MT) of the kernel for M
   int per_sm;                 // CTAs per SM: 2 when two one-set CTAs fit an SM
   int tile0[kMaxLayers + 1];  // first global tile of each layer; tile0[n] = n_tiles
@@ -1090,9 +1114,15 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
   const long long total = static_cast<long long>(p.n_tiles) * p.S;
   if (total >= (1ll << 31)) return false;
   p.total = static_cast<int>(total);
-  p.slot_bytes = slot_bytes_for(M);
   const size_t table = w[0].format != EXQ_FMT_GPTQ4 ? align_up(static_cast<size_t>(n) * (p.S + 1) * 4, 16) : 0;
   const size_t fixed = 512 + table + 1024;  // barriers and descriptors, the segment tables, alignment slack
+  // EXL2 stages of 40 rows where two such slots fit half an SM;
+  // EXQ_GEMV_ROWS=32 keeps them at 32 (a test hook: both heights are tested)
+  const char* rows_env = std::getenv("EXQ_GEMV_ROWS");
+  const bool long_fits = w[0].format != EXQ_FMT_GPTQ4 && M <= 8 &&
+                         2 * static_cast<size_t>(slot_bytes_for(M, kRowsLong)) + fixed <= static_cast<size_t>(kSmemHalf);
+  p.rows = long_fits && !(rows_env && std::atoi(rows_env) == kRowsShort) ? kRowsLong : kRowsShort;
+  p.slot_bytes = slot_bytes_for(M, p.rows);
   // one set per CTA and two CTAs per SM where a ring of two slots fits half
   // the shared memory (M <= 8): a CTA of the next call can then start on an
   // SM while the other CTA there still works on this one
@@ -1121,7 +1151,7 @@ bool make_plan(const exq_weight* w, int n, int M, int sm_count, Plan& p) {
 }
 
 std::mutex g_attr_mutex;
-bool g_attr_done[64][12];
+bool g_attr_done[64][24];
 
 }  // namespace
 
@@ -1146,10 +1176,11 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
     return EXQ_ERR_INVALID_ARG;
   const exq_weight& w0 = w[0];
 
-  KernelFn fn = pick_kernel(w0.format, M, plan.gather);
+  const bool long_rows = plan.rows == kRowsLong;
+  KernelFn fn = pick_kernel(w0.format, M, plan.gather, long_rows);
   {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
-    bool& done = g_attr_done[dev][variant_index(w0.format, M, plan.gather)];
+    bool& done = g_attr_done[dev][variant_index(w0.format, M, plan.gather, long_rows)];
     if (!done) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta) != cudaSuccess ||
           cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
@@ -1207,7 +1238,7 @@ exq_status launch_gemv(const exq_weight* w, int n, const uint16_t* x, int M, uin
     // another time). 64-byte promotion cut the DRAM reads of a 70B gate+up
     // call from 1.146 to 1.091 times the packed bytes.
     if (!encode_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[i].qweight, w[i].N, w[i].n_word_rows,
-                   static_cast<uint64_t>(w[i].N) * 4, kTN, kRowsPerStage, CU_TENSOR_MAP_L2_PROMOTION_L2_64B))
+                   static_cast<uint64_t>(w[i].N) * 4, kTN, plan.rows, CU_TENSOR_MAP_L2_PROMOTION_L2_64B))
       return EXQ_ERR_CUDA;
     // fp16 scale rows (two-level scales come without a tensor map)
     if (w[i].scales && !encode_2d(&maps.s[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, w[i].scales, w[i].N, scale_rows,

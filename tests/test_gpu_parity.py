@@ -120,6 +120,26 @@ def test_gemv_exl2_small(env, M, K, N, bits, perm):
     check_matmul(y, O.matmul(x, oracle_W_exl2(e)), f"exl2 K={K} N={N} M={M}")
 
 
+@pytest.mark.parametrize("rows", [32, 40])
+@pytest.mark.parametrize("K,N,bits,perm", EXL2_SMALL + [(4096, 520, 3.0, True)])
+def test_gemv_exl2_both_stage_heights(env, rows, K, N, bits, perm, monkeypatch):
+    # EXL2 stages of 32 or 40 word rows: the one-set kernel (M <= 8) takes
+    # 40 where two such slots fit half an SM, and the test hook keeps them at
+    # 32; both on every SM and on 3 CTAs (several stages and pieces per CTA)
+    exq, torch = env
+    monkeypatch.setenv("EXQ_GEMV_ROWS", str(rows))
+    kw = dict(bits=bits) if isinstance(bits, np.ndarray) else dict(bpw=bits, allowed=(2, 3, 4) if bits < 3 else synth.EXL2_BITS)
+    e = exl2_case(K, N, permute=perm, seed=K + N + rows, **kw)
+    w = _exl2_dev(exq, e)
+    W_ref = oracle_W_exl2(e)
+    for ctas in (None, 3):
+        if ctas:
+            monkeypatch.setenv("EXQ_GEMV_CTAS", str(ctas))
+        for M in (1, 4):
+            x = synth.activations(M, K, seed=M + rows)
+            check_matmul(_gemv(exq, torch, w, x), O.matmul(x, W_ref), f"rows={rows} ctas={ctas} K={K} N={N} M={M}")
+
+
 def test_gemv_one_hot_rows_exact(env):
     # x = e_k reproduces row k of the dequantized weight exactly (fp32 sum of
     # one product, rounded back to fp16)

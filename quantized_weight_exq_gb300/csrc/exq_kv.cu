@@ -19,6 +19,8 @@
 // as one contiguous block (D * 2 bytes of fp16, D * b / 8 bytes of codes); all
 // of a warp's loads are issued before any of its arithmetic, to keep enough
 // bytes in flight per SM.
+#include <type_traits>
+
 #include "exq_device.cuh"
 #include "exq_internal.h"
 
@@ -42,6 +44,17 @@ __device__ __forceinline__ float div_by_const(float x) {
   const float q = __fmul_rn(x, y);
   const float r = __fmaf_rn(-q, static_cast<float>(C), x);
   return __fmaf_rn(r, y, q);
+}
+
+// 1 / s from the hardware's approximate reciprocal (PTX `rcp.approx.ftz.f32`,
+// at most 1 ulp from 1 / s over the whole range; s is an fp16 value, so
+// never an fp32 subnormal). x * inv is then within |x / s| 2^-22 of
+// fp32_RN(x / s): 2^-15 for the codes that are not clamped (|x / s| <=
+// 128), half the window below in which the exact quotient decides.
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
 template <int VPL>  // values per lane: D / 32
@@ -155,15 +168,26 @@ __global__ void __launch_bounds__(kWarps * 32)
     static_assert(kQmax == 7 || kQmax == 31 || kQmax == 127, "div_by_const is checked for these only");
     const __half s16 = __float2half_rn(div_by_const<kQmax>(amax));
     const float s = __half2float(s16);
-    const float inv = s != 0.f ? __frcp_rn(s) : 0.f;
+    const float inv = s != 0.f ? rcp_approx(s) : 0.f;  // s = 0: every q is 0
 
-    unsigned long long chunk = 0;
+    // q = rint(fp32_RN(x / s)): from x * inv, except where that lies within
+    // 2^-14 of a half-integer; one test per lane for its VPL values
+    int q[VPL];
+    bool near_tie = false;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      int q = 0;
-      if (s != 0.f) q = max(-kQmax - 1, min(kQmax, round_quotient(xf[i], s, inv)));
-      chunk |= static_cast<unsigned long long>(q + (1 << (B - 1))) << (i * B);
+      const float r = xf[i] * inv;
+      q[i] = __float2int_rn(r);
+      near_tie |= fabsf(r - static_cast<float>(q[i])) > 0.5f - 0x1p-14f;
     }
+    if (near_tie)
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) q[i] = __float2int_rn(__fdiv_rn(xf[i], s));
+    using Chunk = std::conditional_t<(kChunk <= 32), uint32_t, unsigned long long>;
+    Chunk chunk = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      chunk |= static_cast<Chunk>(max(-kQmax - 1, min(kQmax, q[i])) + (1 << (B - 1))) << (i * B);
     store_words<kChunk, kWords>(chunk, codes + g * kWords, lane);
     if (lane == 0) scales[g] = __half_as_ushort(s16);
   }

@@ -96,6 +96,12 @@ __device__ __forceinline__ void store_words(unsigned long long chunk, uint32_t* 
   } else if constexpr (kChunk == 32) {  // one whole word per lane
     dst[lane] = static_cast<uint32_t>(chunk);
     return;
+  } else if constexpr (kChunk == 24) {  // four lanes fill three words: lane 4k + i (i < 3) writes word 3k + i
+    const uint32_t c = static_cast<uint32_t>(chunk);
+    const uint32_t next = __shfl_down_sync(0xffffffffu, c, 1);
+    const int i = lane & 3;
+    if (i < 3) dst[3 * (lane >> 2) + i] = (c >> (8 * i)) | (next << (24 - 8 * i));
+    return;
   } else if constexpr (kChunk == 16 || kChunk == 8) {  // 32 / kChunk lanes fill a word
     constexpr int kPer = 32 / kChunk;
     uint32_t word = static_cast<uint32_t>(chunk);

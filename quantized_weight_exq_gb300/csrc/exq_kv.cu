@@ -189,11 +189,18 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (near_tie)
 #pragma unroll
       for (int i = 0; i < VPL; ++i) q[i] = __float2int_rn(__fdiv_rn(xf[i], s));
+    // A normal fp16 s is within 2^-11 (plus the fp32 quotient's 2^-24) of
+    // amax / qmax, so |x / s| < qmax (1 + 2^-10) < qmax + 1/2 and every q is
+    // already in range; only a subnormal s (amax < 2^-14 qmax), with fewer
+    // significant bits, needs the clamp. The test is the same for the whole
+    // warp (s is the group's).
+    if (s < 0x1p-14f)
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) q[i] = max(-kQmax - 1, min(kQmax, q[i]));
     using Chunk = std::conditional_t<(kChunk <= 32), uint32_t, unsigned long long>;
     Chunk chunk = 0;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      chunk |= static_cast<Chunk>(max(-kQmax - 1, min(kQmax, q[i])) + (1 << (B - 1))) << (i * B);
+    for (int i = 0; i < VPL; ++i) chunk |= static_cast<Chunk>(q[i] + (1 << (B - 1))) << (i * B);
     store_words<kChunk, kWords>(chunk, codes + g * kWords, lane);
     if (lane == 0) scales[g] = __half_as_ushort(s16);
   }

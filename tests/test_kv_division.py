@@ -57,3 +57,19 @@ def test_kernel_reciprocals_are_the_rounded_ones():
     assert m, "div_by_const's constants not found"
     for c, hx in zip((7, 31, 127), m.groups()):
         assert Fraction(float.fromhex(hx)) == _rn32(Fraction(1, c)), (c, hx)
+
+
+@pytest.mark.parametrize("qmax", [7, 31, 127])
+def test_normal_scale_keeps_codes_in_range(qmax):
+    # The write kernel clamps q only for subnormal scales. For every positive
+    # finite fp16 amax whose scale s = fp16_RN(fp32_RN(amax / qmax)) is a
+    # normal fp16, amax / s stays below qmax + 1/2 by more than the 2^-15 by
+    # which the kernel's quotient may differ from fp32_RN(x / s), so
+    # rint(x / s) is within [-qmax, qmax] for every |x| <= amax. Exhaustive
+    # over the fp16 magnitudes, exact rational arithmetic for the ratio.
+    h = np.arange(1, 0x7C00, dtype=np.uint16).view(np.float16)
+    s = (h.astype(np.float32) / np.float32(qmax)).astype(np.float16)
+    normal = s.astype(np.float64) >= 2.0 ** -14
+    assert normal.any()
+    worst = max(Fraction(float(a)) / Fraction(float(b)) for a, b in zip(h[normal], s[normal]))
+    assert worst + Fraction(1, 2 ** 15) < Fraction(2 * qmax + 1, 2), (qmax, float(worst))

@@ -59,6 +59,42 @@ def test_kv_codec_bit_exact(env, D, bits):
     assert np.array_equal(_bits16(out), O.kv_dequantize(w_ref, s_ref, bits, D))
 
 
+def _tie_groups(G, D, bits, seed):
+    """Groups whose quotients x / s are half-integers or one fp16 step away
+    from one: the scale s0 = (1 + j/4) 2^e has three significant bits, the
+    maximum qmax s0 is one of the values (so s = s0 exactly), and every other
+    value is (k + 1/2) s0 for k in [-qmax, qmax - 1], exact in fp16, or its
+    fp16 neighbour above or below. Every such value sits in the window where
+    the write path takes the exact division, or just outside it."""
+    rng = np.random.default_rng(seed)
+    qmax = (1 << (bits - 1)) - 1
+    s0 = (1 + rng.integers(0, 4, G) / 4) * np.exp2(rng.integers(-10, 3, G).astype(np.float64))
+    k = rng.integers(-qmax, qmax, (G, D))
+    x = ((k + 0.5) * s0[:, None]).astype(np.float16)
+    assert np.array_equal(x.astype(np.float64), (k + 0.5) * s0[:, None])  # the ties are exact
+    step = rng.integers(-1, 2, (G, D))                                       # -1, 0 or +1 fp16 step
+    bits16 = x.view(np.uint16).astype(np.int64)
+    sign = np.where(x < 0, -1, 1)
+    x = (bits16 + step * sign).astype(np.uint16).view(np.float16)
+    x[np.arange(G), rng.integers(0, D, G)] = (qmax * s0).astype(np.float16)
+    assert np.array_equal(np.abs(x.astype(np.float64)).max(axis=1), qmax * s0)
+    return x
+
+
+@pytest.mark.parametrize("bits", [4, 6, 8])
+def test_kv_quotient_ties_and_neighbours(env, bits):
+    # the write path rounds x / s from a multiply by an approximate 1 / s and
+    # takes the exact division only near half-integers; here nearly every
+    # value is an exact tie (to even) or one fp16 step from one
+    exq, torch = env
+    x = _tie_groups(4096, 128, bits, seed=bits)
+    codes, scales = exq.exq_kv_quantize(torch.from_numpy(x).cuda(), bits)
+    u_ref, s_ref = O.kv_quantize(x, bits)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits16(scales), s_ref)
+    assert np.array_equal(codes.cpu().numpy().view(np.uint32), O.kv_pack(u_ref, bits))
+
+
 def test_kv_dequantize_of_oracle_codes(env):
     # the read path alone, on codes and scales written by the oracle
     exq, torch = env
